@@ -1,0 +1,331 @@
+"""CPU oracle for the fused DiT chains -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+and reference arms may import this package.  The CUDA library and its
+Python binding never touch it; the two share no code.
+
+The arithmetic lives in ``oracle.c`` (plain scalar C, IEEE binary32 with
+explicit ``fmaf``, built with ``-ffp-contract=off``); this module only
+compiles it with gcc and marshals numpy arrays.  Every array of storage
+values is ``uint16`` (bf16 or fp16 bit patterns).  Each function cites the
+passage it follows in ``oracle.c``.
+
+Parity status of each function (what pins it, see ``tests/test_oracle_*``):
+  ln_modulate        pinned: fp64 two-pass LayerNorm, exact-arithmetic
+                     cases, modulate identities, bit-level symmetries
+  qk_head_layernorm  pinned: fp64 two-pass LayerNorm with affine, exact cases
+  residual_gate_add  pinned: single-rounding fp64 definition
+  bias_gelu_tanh     pinned: 100-bit evaluation of tanh-GELU on all inputs
+  rsqrt_cr           pinned: 100-bit evaluation
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_DEFAULT_LIB = _LIB_PATH
+CFLAGS = ["-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fno-builtin",
+          "-Wall", "-shared", "-fPIC"]
+_lib = None
+_lock = threading.Lock()
+
+DTYPE_CODE = {"bf16": 0, "fp16": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``oracle/_build/liboracle.so`` (if stale)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+_F = ctypes.c_float
+_INT = ctypes.c_int
+
+
+def _lib_handle():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build() if _LIB_PATH == _DEFAULT_LIB else _LIB_PATH)
+            sig = {
+                "oracle_ln_modulate": [_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _I, _F, _INT,
+                                       _I, _I, _P, _P],
+                "oracle_qk_head_layernorm": [_P, _P, _I, _I, _P, _P, _F, _INT, _I, _I],
+                "oracle_residual_gate_add": [_P, _P, _P, _I, _P, _I, _I, _I, _INT, _I, _I],
+                "oracle_bias_gelu_tanh": [_P, _P, _P, _I, _I, _INT, _I, _I],
+                "oracle_gelu_table": [_P, _INT],
+                "oracle_row_stats": [_P, _I, _INT, _P, _P],
+            }
+            for name, args in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            for name, args in {"oracle_f32_to_16": [_P, _P, _I, _INT],
+                               "oracle_16_to_f32": [_P, _P, _I, _INT],
+                               "oracle_rsqrt_cr_array": [_P, _P, _I]}.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = None
+            lib.oracle_rsqrt_cr.argtypes = [_F]
+            lib.oracle_rsqrt_cr.restype = _F
+            _lib = lib
+    return _lib
+
+
+class loaded_from:
+    """Context manager: route every call of this module to another build of
+    the oracle (used by the test that plants mistakes in a copy of
+    ``oracle.c`` and checks that the pins catch them)."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self.saved = (_lib, dict(_tables))
+        _lib = None
+        _tables.clear()
+        real = _LIB_PATH
+        globals()["_LIB_PATH"] = self.path
+        try:
+            _lib_handle()
+        finally:
+            globals()["_LIB_PATH"] = real
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib, tables = self.saved
+        _tables.clear()
+        _tables.update(tables)
+        return False
+
+
+
+def _u16(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("storage arrays are uint16 bit patterns")
+    return a
+
+
+def _segments(rows: Optional[Sequence[int]], total: int) -> Tuple[np.ndarray, list]:
+    """Sorted row indices and their maximal contiguous runs [(begin, end), ...]."""
+    if rows is None:
+        idx = np.arange(total, dtype=np.int64)
+    else:
+        idx = np.asarray(sorted(set(int(r) for r in rows)), dtype=np.int64)
+        if idx.size and (idx[0] < 0 or idx[-1] >= total):
+            raise IndexError("row index out of range")
+    runs = []
+    if idx.size:
+        start = prev = int(idx[0])
+        for r in idx[1:]:
+            r = int(r)
+            if r != prev + 1:
+                runs.append((start, prev + 1))
+                start = r
+            prev = r
+        runs.append((start, prev + 1))
+    return idx, runs
+
+
+def _split_runs(runs, threads: int):
+    """Split runs into about `threads` pieces of similar size for a pool."""
+    total = sum(e - b for b, e in runs)
+    if threads <= 1 or total < 2 * threads:
+        return runs
+    step = max(1, total // (threads * 4))
+    out = []
+    for b, e in runs:
+        while b < e:
+            out.append((b, min(e, b + step)))
+            b += step
+    return out
+
+
+def _run(pieces, fn, threads):
+    if threads <= 1 or len(pieces) <= 1:
+        for p in pieces:
+            fn(p)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as pool:
+            list(pool.map(fn, pieces))
+
+
+# --------------------------------------------------------------------------
+# the four chains
+# --------------------------------------------------------------------------
+
+def ln_modulate(x_base: np.ndarray, B: int, N: int, D: int, strides: Tuple[int, int, int],
+                scale_base: np.ndarray, scale_offset: int, s_scale_b: int,
+                shift_base: np.ndarray, shift_offset: int, s_shift_b: int,
+                eps: float, dtype: str = "bf16", rows: Optional[Sequence[int]] = None,
+                threads: int = 1, return_stats: bool = False):
+    """LayerNorm (no affine) + adaLN modulate on rows ``r = b*N + n``.
+
+    ``x_base`` is the flat storage buffer; element (b, n, d) sits at
+    ``b*sxB + n*sxN + d*sxD``.  ``scale``/``shift`` row b starts at
+    ``offset + b*s_b`` of their buffers.  Returns ``(row_ids, out)`` with
+    ``out`` of shape ``(len(row_ids), D)``; with ``return_stats`` also the
+    per-row binary32 mean and rstd.
+    """
+    lib = _lib_handle()
+    xb, sb, hb = _u16(x_base).reshape(-1), _u16(scale_base).reshape(-1), _u16(shift_base).reshape(-1)
+    idx, runs = _segments(rows, B * N)
+    out = np.zeros((idx.size, D), dtype=np.uint16)
+    mean = np.zeros(idx.size, dtype=np.float32)
+    rstd = np.zeros(idx.size, dtype=np.float32)
+    pos = {int(r): i for i, r in enumerate(idx)}
+    sxB, sxN, sxD = strides
+    pieces = _split_runs(runs, threads)
+
+    def one(piece):
+        b0, e0 = piece
+        i0 = pos[b0]
+        rc = lib.oracle_ln_modulate(out[i0:].ctypes.data, xb.ctypes.data, B, N, D, sxB, sxN, sxD,
+                                    sb.ctypes.data + 2 * scale_offset, s_scale_b,
+                                    hb.ctypes.data + 2 * shift_offset, s_shift_b, eps,
+                                    DTYPE_CODE[dtype], b0, e0, mean[i0:].ctypes.data,
+                                    rstd[i0:].ctypes.data)
+        if rc:
+            raise ValueError(f"oracle_ln_modulate rejected its arguments ({rc})")
+
+    _run(pieces, one, threads)
+    if return_stats:
+        return idx, out, mean, rstd
+    return idx, out
+
+
+def qk_head_layernorm(x: np.ndarray, Dh: int, w: np.ndarray, b: np.ndarray, eps: float,
+                      dtype: str = "bf16", rows: Optional[Sequence[int]] = None,
+                      threads: int = 1):
+    """Per-head LayerNorm with affine on a (rows, Dh) tensor; returns (row_ids, out)."""
+    lib = _lib_handle()
+    xf = _u16(x).reshape(-1)
+    nrows = xf.size // Dh
+    w, b = _u16(w).reshape(-1), _u16(b).reshape(-1)
+    idx, runs = _segments(rows, nrows)
+    out = np.zeros((idx.size, Dh), dtype=np.uint16)
+    pos = {int(r): i for i, r in enumerate(idx)}
+
+    def one(piece):
+        b0, e0 = piece
+        rc = lib.oracle_qk_head_layernorm(out[pos[b0]:].ctypes.data, xf.ctypes.data, nrows, Dh,
+                                          w.ctypes.data, b.ctypes.data, eps, DTYPE_CODE[dtype],
+                                          b0, e0)
+        if rc:
+            raise ValueError(f"oracle_qk_head_layernorm rejected its arguments ({rc})")
+
+    _run(_split_runs(runs, threads), one, threads)
+    return idx, out
+
+
+def residual_gate_add(x: np.ndarray, gate_base: np.ndarray, gate_offset: int, s_gate_b: int,
+                      y: np.ndarray, B: int, N: int, D: int, dtype: str = "bf16",
+                      rows: Optional[Sequence[int]] = None, threads: int = 1):
+    """``x + gate*y`` with per-op storage rounding; returns (row_ids, out)."""
+    lib = _lib_handle()
+    xf, yf, gf = _u16(x).reshape(-1), _u16(y).reshape(-1), _u16(gate_base).reshape(-1)
+    idx, runs = _segments(rows, B * N)
+    out = np.zeros((idx.size, D), dtype=np.uint16)
+    pos = {int(r): i for i, r in enumerate(idx)}
+
+    def one(piece):
+        b0, e0 = piece
+        lib.oracle_residual_gate_add(out[pos[b0]:].ctypes.data, xf.ctypes.data,
+                                     gf.ctypes.data + 2 * gate_offset, s_gate_b, yf.ctypes.data,
+                                     B, N, D, DTYPE_CODE[dtype], b0, e0)
+
+    _run(_split_runs(runs, threads), one, threads)
+    return idx, out
+
+
+def bias_gelu_tanh(x: np.ndarray, bias: np.ndarray, rows_total: int, width: int,
+                   dtype: str = "bf16", rows: Optional[Sequence[int]] = None,
+                   threads: int = 1):
+    """``gelu_tanh(round(x + bias))`` rounded to storage; returns (row_ids, out)."""
+    lib = _lib_handle()
+    xf, bf = _u16(x).reshape(-1), _u16(bias).reshape(-1)
+    idx, runs = _segments(rows, rows_total)
+    out = np.zeros((idx.size, width), dtype=np.uint16)
+    pos = {int(r): i for i, r in enumerate(idx)}
+    gelu_table(dtype)  # build the table once, before any threads start
+
+    def one(piece):
+        b0, e0 = piece
+        lib.oracle_bias_gelu_tanh(out[pos[b0]:].ctypes.data, xf.ctypes.data, bf.ctypes.data,
+                                  rows_total, width, DTYPE_CODE[dtype], b0, e0)
+
+    _run(_split_runs(runs, threads), one, threads)
+    return idx, out
+
+
+_tables = {}
+
+
+def gelu_table(dtype: str = "bf16") -> np.ndarray:
+    """All 65536 outputs ``round16(G(v))`` indexed by the pattern of v."""
+    if dtype not in _tables:
+        t = np.zeros(65536, dtype=np.uint16)
+        _lib_handle().oracle_gelu_table(t.ctypes.data, DTYPE_CODE[dtype])
+        # also warm the C side's own copy used by oracle_bias_gelu_tanh
+        one = np.zeros(1, dtype=np.uint16)
+        _lib_handle().oracle_bias_gelu_tanh(one.ctypes.data, one.ctypes.data, one.ctypes.data,
+                                            1, 1, DTYPE_CODE[dtype], 0, 1)
+        _tables[dtype] = t
+    return _tables[dtype]
+
+
+# --------------------------------------------------------------------------
+# helpers used by the oracle's own pins
+# --------------------------------------------------------------------------
+
+def to16(f: np.ndarray, dtype: str = "bf16") -> np.ndarray:
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    out = np.empty(f.shape, dtype=np.uint16)
+    _lib_handle().oracle_f32_to_16(f.ctypes.data, out.ctypes.data, f.size, DTYPE_CODE[dtype])
+    return out
+
+
+def from16(h: np.ndarray, dtype: str = "bf16") -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.float32)
+    _lib_handle().oracle_16_to_f32(h.ctypes.data, out.ctypes.data, h.size, DTYPE_CODE[dtype])
+    return out
+
+
+def rsqrt_cr(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    _lib_handle().oracle_rsqrt_cr_array(x.ctypes.data, out.ctypes.data, x.size)
+    return out
+
+
+def row_stats(row: np.ndarray, lanes: int = 128) -> Tuple[float, float]:
+    """(mean, m2) of one binary32 row on the canonical lane DAG."""
+    row = np.ascontiguousarray(row, dtype=np.float32)
+    m = np.zeros(1, dtype=np.float32)
+    q = np.zeros(1, dtype=np.float32)
+    rc = _lib_handle().oracle_row_stats(row.ctypes.data, row.size, lanes, m.ctypes.data,
+                                        q.ctypes.data)
+    if rc:
+        raise ValueError("bad row length / lane count")
+    return float(m[0]), float(q[0])
