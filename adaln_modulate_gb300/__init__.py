@@ -1,0 +1,226 @@
+"""Python binding of ``libadaln_gb300.so`` (the C ABI in ``include/adaln.h``).
+
+Argument marshalling only: every operation runs in the library's sm_103a
+kernels.  There is no fallback: if the library is not built, importing this
+package raises ``ImportError`` (build it with ``__graft_entry__.build()`` or
+``python adaln_modulate_gb300/_build.py``).
+
+Two layers:
+  * ``capi``: the C functions under their C names (``capi.adaln_ln_modulate``
+    and so on), taking raw integers (device pointers, sizes, a stream handle);
+  * ``ln_modulate``, ``qk_head_layernorm``, ``residual_gate_add``,
+    ``bias_gelu_tanh``: the same calls taking torch tensors (PyTorch only
+    provides the device memory and the current stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+from . import _build
+
+LIB_PATH = _build.LIB
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "adaln.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build() (nvcc, sm_103a)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+BF16, FP16 = 0, 1
+FLAG_PDL = 1
+STATUS = {0: "ADALN_OK", 1: "ADALN_E_NULL", 2: "ADALN_E_DTYPE", 3: "ADALN_E_SHAPE",
+          4: "ADALN_E_ALIGN", 5: "ADALN_E_STRIDE", 6: "ADALN_E_VALUE", 7: "ADALN_E_OVERLAP",
+          8: "ADALN_E_CUDA"}
+VARIANTS = {0: "rows", 1: "tokens", 2: "generic"}
+
+_P, _I, _F, _U, _INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_uint32, ctypes.c_int
+_SIGS = {
+    "adaln_status_str": ([_INT], ctypes.c_char_p),
+    "adaln_last_cuda_error": ([], ctypes.c_char_p),
+    "adaln_version": ([], _INT),
+    "adaln_init": ([_INT], _INT),
+    "adaln_shutdown": ([], _INT),
+    "adaln_ln_modulate": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U, _P], _INT),
+    "adaln_can_ln_modulate": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U], _INT),
+    "adaln_ln_modulate_variant": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U],
+                                  _INT),
+    "adaln_qk_head_layernorm": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _F, _INT, _U, _P], _INT),
+    "adaln_can_qk_head_layernorm": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _F, _INT, _U],
+                                    _INT),
+    "adaln_residual_gate_add": ([_P, _P, _P, _I, _P, _I, _I, _I, _INT, _U, _P], _INT),
+    "adaln_can_residual_gate_add": ([_P, _P, _P, _I, _P, _I, _I, _I, _INT, _U], _INT),
+    "adaln_bias_gelu_tanh": ([_P, _P, _P, _I, _I, _INT, _U, _P], _INT),
+    "adaln_can_bias_gelu_tanh": ([_P, _P, _P, _I, _I, _INT, _U], _INT),
+}
+
+
+class _CApi:
+    """The C entry points under their C names."""
+
+    def __init__(self, lib):
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+            setattr(self, name, fn)
+
+
+capi = _CApi(_lib)
+
+
+def header_functions() -> list:
+    """Names of every function declared in include/adaln.h."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(adaln_\w+)\s*\(", text)))
+
+
+class AdalnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = f"{where}: {STATUS.get(status, status)}"
+        if status == 8:
+            msg += f" ({capi.adaln_last_cuda_error().decode()})"
+        super().__init__(msg)
+        self.status = status
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise AdalnError(status, where)
+
+
+# ------------------------------------------------------------------ torch
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float16:
+        return FP16
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 / fp16 only)")
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _rows_view(t, D: int, name: str):
+    """(pointer, batch stride) of a (B, D) / (B, 1, D) row tensor."""
+    if t.dim() == 3:
+        if t.shape[1] != 1:
+            raise ValueError(f"{name} must be (B, 1, D)")
+        t = t[:, 0]
+    if t.dim() == 1:
+        t = t.unsqueeze(0)
+    if t.dim() != 2 or t.shape[-1] != D or (D > 1 and t.stride(-1) != 1):
+        raise ValueError(f"{name} must be (B, D) rows contiguous over D")
+    return t.data_ptr(), (t.stride(0) if t.shape[0] > 1 else 0)
+
+
+def ln_modulate(x, scale, shift, eps: float, out=None, flags: int = 0, stream=None):
+    """``LN(x) * (1 + scale) + shift`` for x (B, N, D) of any strides;
+    scale / shift (B, 1, D) or (B, D) with contiguous rows.  Returns the
+    contiguous (B, N, D) output."""
+    torch = _torch()
+    B, N, D = x.shape
+    if out is None:
+        out = torch.empty((B, N, D), dtype=x.dtype, device=x.device)
+    sp, ssb = _rows_view(scale, D, "scale")
+    hp, hsb = _rows_view(shift, D, "shift")
+    if scale.shape[0] not in (1, B) or shift.shape[0] not in (1, B):
+        raise ValueError("scale / shift batch must be 1 or B")
+    if scale.shape[0] == 1:
+        ssb = 0
+    if shift.shape[0] == 1:
+        hsb = 0
+    st = capi.adaln_ln_modulate(out.data_ptr(), x.data_ptr(), B, N, D, *x.stride(), sp, ssb, hp,
+                                hsb, float(eps), _dtype_code(x), flags, _stream(stream))
+    _check(st, "adaln_ln_modulate")
+    return out
+
+
+def ln_modulate_variant(x, scale, shift, eps: float, out=None) -> str:
+    """Which kernel ln_modulate takes for these tensors (no CUDA work)."""
+    B, N, D = x.shape
+    sp, ssb = _rows_view(scale, D, "scale")
+    hp, hsb = _rows_view(shift, D, "shift")
+    optr = out.data_ptr() if out is not None else 1 << 40
+    v = capi.adaln_ln_modulate_variant(optr, x.data_ptr(), B, N, D, *x.stride(), sp, ssb, hp, hsb,
+                                       float(eps), _dtype_code(x), 0)
+    if v < 0:
+        raise AdalnError(-v, "adaln_ln_modulate_variant")
+    return VARIANTS[v]
+
+
+def qk_head_layernorm(q, k, wq, bq, wk, bk, eps: float, q_out=None, k_out=None, flags: int = 0,
+                      stream=None):
+    """Per-head LayerNorm with affine of q and k (any leading shape, last
+    dim Dh, contiguous) in one launch.  Pass ``q_out=q`` for in place."""
+    torch = _torch()
+    Dh = q.shape[-1] if q is not None else k.shape[-1]
+    rq = q.numel() // Dh if q is not None else 0
+    rk = k.numel() // Dh if k is not None else 0
+    for t in (q, k):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("q / k must be contiguous")
+    if q is not None and q_out is None:
+        q_out = torch.empty_like(q)
+    if k is not None and k_out is None:
+        k_out = torch.empty_like(k)
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    ref = q if q is not None else k
+    st = capi.adaln_qk_head_layernorm(ptr(q_out), ptr(q), rq, ptr(k_out), ptr(k), rk, Dh, ptr(wq),
+                                      ptr(bq), ptr(wk), ptr(bk), float(eps), _dtype_code(ref), flags,
+                                      _stream(stream))
+    _check(st, "adaln_qk_head_layernorm")
+    return q_out, k_out
+
+
+def residual_gate_add(x, gate, y, out=None, flags: int = 0, stream=None):
+    """``x + gate * y`` for contiguous x, y (B, N, D) and gate (B, 1, D) / (B, D)."""
+    torch = _torch()
+    B, N, D = x.shape
+    if not (x.is_contiguous() and y.is_contiguous()) or y.shape != x.shape:
+        raise ValueError("x and y must be contiguous (B, N, D)")
+    if out is None:
+        out = torch.empty_like(x)
+    gp, gsb = _rows_view(gate, D, "gate")
+    if gate.shape[0] == 1:
+        gsb = 0
+    st = capi.adaln_residual_gate_add(out.data_ptr(), x.data_ptr(), gp, gsb, y.data_ptr(), B, N, D,
+                                      _dtype_code(x), flags, _stream(stream))
+    _check(st, "adaln_residual_gate_add")
+    return out
+
+
+def bias_gelu_tanh(x, bias, out=None, flags: int = 0, stream=None):
+    """``gelu_tanh(round(x + bias))`` for contiguous x (..., width), bias (width,)."""
+    torch = _torch()
+    width = x.shape[-1]
+    if not x.is_contiguous() or bias.numel() != width or not bias.is_contiguous():
+        raise ValueError("x contiguous (..., width), bias (width,)")
+    if out is None:
+        out = torch.empty_like(x)
+    st = capi.adaln_bias_gelu_tanh(out.data_ptr(), x.data_ptr(), bias.data_ptr(),
+                                   x.numel() // width, width, _dtype_code(x), flags, _stream(stream))
+    _check(st, "adaln_bias_gelu_tanh")
+    return out
+
+
+def init(device: Optional[int] = None) -> None:
+    """Build the per-device GELU tables now (needed before graph capture)."""
+    if device is None:
+        device = _torch().cuda.current_device()
+    _check(capi.adaln_init(int(device)), "adaln_init")

@@ -1,0 +1,366 @@
+// C ABI of the library: argument validation, per-device state, dispatch.
+// Declared in include/adaln.h; every entry point is extern "C", takes plain
+// pointers and sizes, and validates everything on the host before the first
+// CUDA call.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/adaln.h"
+#include "kernels.h"
+
+using namespace adaln;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DevState {
+    DeviceInfo info;
+    bool have_info = false;
+    void *gelu = nullptr;  // 2 x 65536 storage values: bf16 table then fp16 table
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+thread_local char g_err[256] = "";
+
+adaln_status cuda_fail(cudaError_t e) {
+    snprintf(g_err, sizeof(g_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return ADALN_E_CUDA;
+}
+
+adaln_status current_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (*dev < 0 || *dev >= kMaxDevices) {
+        snprintf(g_err, sizeof(g_err), "device ordinal %d beyond %d", *dev, kMaxDevices);
+        return ADALN_E_CUDA;
+    }
+    return ADALN_OK;
+}
+
+// device properties, cached (the caller holds no lock)
+adaln_status device_info(int dev, DeviceInfo *out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState &d = g_dev[dev];
+    if (!d.have_info) {
+        int sms = 0, smem = 0, l2 = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        d.info.device = dev;
+        d.info.sms = sms;
+        d.info.max_smem_optin = smem;
+        d.info.l2_bytes = l2;
+        d.have_info = true;
+    }
+    *out = d.info;
+    return ADALN_OK;
+}
+
+// builds the GELU tables of the current device (g_mu held by the caller)
+adaln_status build_tables_locked(int dev) {
+    DevState &d = g_dev[dev];
+    if (d.gelu) return ADALN_OK;
+    void *buf = nullptr;
+    cudaError_t e = cudaMalloc(&buf, 2 * 65536 * sizeof(uint16_t));
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaStream_t s = nullptr;
+    e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = launch_gelu_table_init(buf, 0, s);
+    if (e == cudaSuccess) e = launch_gelu_table_init((uint16_t *)buf + 65536, 1, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (s) cudaStreamDestroy(s);
+    if (e != cudaSuccess) {
+        cudaFree(buf);
+        return cuda_fail(e);
+    }
+    d.gelu = buf;
+    return ADALN_OK;
+}
+
+bool finite_nonneg(float v) { return isfinite(v) && v >= 0.0f; }
+bool al2(const void *p) { return ((uintptr_t)p & 1u) == 0; }
+bool al8(const void *p) { return ((uintptr_t)p & 7u) == 0; }
+
+// [a, a+na) and [b, b+nb) in bytes intersect
+bool overlap(const void *a, int64_t na, const void *b, int64_t nb) {
+    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+    return pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
+}
+
+// ------------------------------------------------------------ checks
+
+adaln_status check_ln(const void *out, const void *x, int64_t B, int64_t N, int64_t D, int64_t sxB,
+                      int64_t sxN, int64_t sxD, const void *scale, int64_t s_scale_b, const void *shift,
+                      int64_t s_shift_b, float eps, int dtype, uint32_t flags) {
+    if (dtype != ADALN_BF16 && dtype != ADALN_FP16) return ADALN_E_DTYPE;
+    if (flags & ~ADALN_FLAG_PDL) return ADALN_E_VALUE;
+    if (!out || !x || !scale || !shift) return ADALN_E_NULL;
+    if (B < 1 || N < 1 || D < 4 || D > 65536 || D % 4 != 0) return ADALN_E_SHAPE;
+    if (B > ((int64_t)1 << 40) / N || B * N > ((int64_t)1 << 46) / D) return ADALN_E_SHAPE;
+    if (sxB < 0 || sxN < 0 || sxD < 0 || s_scale_b < 0 || s_shift_b < 0) return ADALN_E_STRIDE;
+    if (!finite_nonneg(eps)) return ADALN_E_VALUE;
+    if (!al2(out) || !al2(x) || !al2(scale) || !al2(shift)) return ADALN_E_ALIGN;
+    const int64_t out_bytes = 2 * B * N * D;
+    const int64_t x_bytes = 2 * ((B - 1) * sxB + (N - 1) * sxN + (D - 1) * sxD + 1);
+    const bool x_contig = sxD == 1 && (N == 1 || sxN == D) && (B == 1 || sxB == N * D);
+    if (overlap(out, out_bytes, x, x_bytes) && !(out == x && x_contig)) return ADALN_E_OVERLAP;
+    if (overlap(out, out_bytes, scale, 2 * ((B - 1) * s_scale_b + D))) return ADALN_E_OVERLAP;
+    if (overlap(out, out_bytes, shift, 2 * ((B - 1) * s_shift_b + D))) return ADALN_E_OVERLAP;
+    return ADALN_OK;
+}
+
+adaln_status check_qk(const void *q_out, const void *q, int64_t rows_q, const void *k_out, const void *k,
+                      int64_t rows_k, int64_t Dh, const void *wq, const void *bq, const void *wk,
+                      const void *bk, float eps, int dtype, uint32_t flags) {
+    if (dtype != ADALN_BF16 && dtype != ADALN_FP16) return ADALN_E_DTYPE;
+    if (flags & ~ADALN_FLAG_PDL) return ADALN_E_VALUE;
+    if (rows_q < 0 || rows_k < 0 || rows_q + rows_k < 1) return ADALN_E_SHAPE;
+    if (Dh < 4 || Dh > 128 || Dh % 4 != 0) return ADALN_E_SHAPE;
+    if (rows_q > ((int64_t)1 << 46) / Dh || rows_k > ((int64_t)1 << 46) / Dh) return ADALN_E_SHAPE;
+    if (rows_q > 0 && (!q_out || !q || !wq || !bq)) return ADALN_E_NULL;
+    if (rows_k > 0 && (!k_out || !k || !wk || !bk)) return ADALN_E_NULL;
+    if (!finite_nonneg(eps)) return ADALN_E_VALUE;
+    const void *ptrs[] = {rows_q ? q_out : nullptr, rows_q ? q : nullptr, rows_q ? wq : nullptr,
+                          rows_q ? bq : nullptr, rows_k ? k_out : nullptr, rows_k ? k : nullptr,
+                          rows_k ? wk : nullptr, rows_k ? bk : nullptr};
+    for (const void *p : ptrs)
+        if (p && !al8(p)) return ADALN_E_ALIGN;
+    const int64_t qb = 2 * rows_q * Dh, kb = 2 * rows_k * Dh, vb = 2 * Dh;
+    if (rows_q) {
+        if (overlap(q_out, qb, q, qb) && q_out != q) return ADALN_E_OVERLAP;
+        if (overlap(q_out, qb, wq, vb) || overlap(q_out, qb, bq, vb)) return ADALN_E_OVERLAP;
+        if (rows_k && (overlap(q_out, qb, k, kb) || overlap(q_out, qb, k_out, kb) ||
+                       overlap(q_out, qb, wk, vb) || overlap(q_out, qb, bk, vb)))
+            return ADALN_E_OVERLAP;
+    }
+    if (rows_k) {
+        if (overlap(k_out, kb, k, kb) && k_out != k) return ADALN_E_OVERLAP;
+        if (overlap(k_out, kb, wk, vb) || overlap(k_out, kb, bk, vb)) return ADALN_E_OVERLAP;
+        if (rows_q && (overlap(k_out, kb, q, qb) || overlap(k_out, kb, wq, vb) || overlap(k_out, kb, bq, vb)))
+            return ADALN_E_OVERLAP;
+    }
+    return ADALN_OK;
+}
+
+adaln_status check_gate(const void *out, const void *x, const void *gate, int64_t s_gate_b, const void *y,
+                        int64_t B, int64_t N, int64_t D, int dtype, uint32_t flags) {
+    if (dtype != ADALN_BF16 && dtype != ADALN_FP16) return ADALN_E_DTYPE;
+    if (flags & ~ADALN_FLAG_PDL) return ADALN_E_VALUE;
+    if (!out || !x || !gate || !y) return ADALN_E_NULL;
+    if (B < 1 || N < 1 || D < 1) return ADALN_E_SHAPE;
+    if (B > ((int64_t)1 << 40) / N || B * N > ((int64_t)1 << 46) / D) return ADALN_E_SHAPE;
+    if (s_gate_b < 0) return ADALN_E_STRIDE;
+    if (!al2(out) || !al2(x) || !al2(gate) || !al2(y)) return ADALN_E_ALIGN;
+    const int64_t nb = 2 * B * N * D;
+    if (overlap(out, nb, x, nb) && out != x) return ADALN_E_OVERLAP;
+    if (overlap(out, nb, y, nb) && out != y) return ADALN_E_OVERLAP;
+    if (overlap(out, nb, gate, 2 * ((B - 1) * s_gate_b + D))) return ADALN_E_OVERLAP;
+    return ADALN_OK;
+}
+
+adaln_status check_gelu(const void *out, const void *x, const void *bias, int64_t rows, int64_t width,
+                        int dtype, uint32_t flags) {
+    if (dtype != ADALN_BF16 && dtype != ADALN_FP16) return ADALN_E_DTYPE;
+    if (flags & ~ADALN_FLAG_PDL) return ADALN_E_VALUE;
+    if (!out || !x || !bias) return ADALN_E_NULL;
+    if (rows < 1 || width < 1 || rows > ((int64_t)1 << 46) / width) return ADALN_E_SHAPE;
+    if (!al2(out) || !al2(x) || !al2(bias)) return ADALN_E_ALIGN;
+    const int64_t nb = 2 * rows * width;
+    if (overlap(out, nb, x, nb) && out != x) return ADALN_E_OVERLAP;
+    if (overlap(out, nb, bias, 2 * width)) return ADALN_E_OVERLAP;
+    return ADALN_OK;
+}
+
+adaln_status finish_launch(cudaError_t e) { return e == cudaSuccess ? ADALN_OK : cuda_fail(e); }
+
+}  // namespace
+
+namespace adaln {
+
+int blocks_per_sm_cached(const void *kernel, int threads, size_t smem) {
+    struct Entry {
+        const void *k;
+        int threads;
+        size_t smem;
+        int n;
+    };
+    static Entry cache[128];
+    static int used = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].k == kernel && cache[i].threads == threads && cache[i].smem == smem) return cache[i].n;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1)
+        n = 1;
+    if (used < 128) cache[used++] = Entry{kernel, threads, smem, n};
+    return n;
+}
+
+}  // namespace adaln
+
+extern "C" {
+
+const char *adaln_status_str(int status) {
+    switch (status) {
+        case ADALN_OK: return "ADALN_OK";
+        case ADALN_E_NULL: return "ADALN_E_NULL: a required pointer is NULL";
+        case ADALN_E_DTYPE: return "ADALN_E_DTYPE: dtype must be ADALN_BF16 or ADALN_FP16";
+        case ADALN_E_SHAPE: return "ADALN_E_SHAPE: a size is out of range";
+        case ADALN_E_ALIGN: return "ADALN_E_ALIGN: a pointer is not aligned";
+        case ADALN_E_STRIDE: return "ADALN_E_STRIDE: a stride is negative";
+        case ADALN_E_VALUE: return "ADALN_E_VALUE: eps negative or not finite, or unknown flags";
+        case ADALN_E_OVERLAP: return "ADALN_E_OVERLAP: an output overlaps an input";
+        case ADALN_E_CUDA: return "ADALN_E_CUDA: a CUDA call failed";
+    }
+    return "unknown adaln_status";
+}
+
+const char *adaln_last_cuda_error(void) { return g_err; }
+
+int adaln_version(void) { return 10000; }
+
+adaln_status adaln_init(int device) {
+    if (device < 0 || device >= kMaxDevices) return ADALN_E_VALUE;
+    int prev = 0;
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return cuda_fail(e);
+    DeviceInfo info;
+    adaln_status st = device_info(device, &info);
+    if (st == ADALN_OK) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        st = build_tables_locked(device);
+    }
+    if (prev != device) cudaSetDevice(prev);
+    return st;
+}
+
+adaln_status adaln_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int prev = 0;
+    cudaGetDevice(&prev);
+    adaln_status st = ADALN_OK;
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (!g_dev[d].gelu) continue;
+        cudaSetDevice(d);
+        cudaError_t e = cudaFree(g_dev[d].gelu);
+        if (e != cudaSuccess) st = cuda_fail(e);
+        g_dev[d].gelu = nullptr;
+    }
+    cudaSetDevice(prev);
+    return st;
+}
+
+adaln_status adaln_can_ln_modulate(const void *out, const void *x, int64_t B, int64_t N, int64_t D,
+                                   int64_t sxB, int64_t sxN, int64_t sxD, const void *scale,
+                                   int64_t s_scale_b, const void *shift, int64_t s_shift_b, float eps,
+                                   int dtype, uint32_t flags) {
+    return check_ln(out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps, dtype, flags);
+}
+
+int adaln_ln_modulate_variant(const void *out, const void *x, int64_t B, int64_t N, int64_t D, int64_t sxB,
+                              int64_t sxN, int64_t sxD, const void *scale, int64_t s_scale_b,
+                              const void *shift, int64_t s_shift_b, float eps, int dtype, uint32_t flags) {
+    adaln_status st =
+        check_ln(out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps, dtype, flags);
+    if (st != ADALN_OK) return -(int)st;
+    LnArgs a{(void *)out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps};
+    return ln_modulate_path(a);
+}
+
+adaln_status adaln_ln_modulate(void *out, const void *x, int64_t B, int64_t N, int64_t D, int64_t sxB,
+                               int64_t sxN, int64_t sxD, const void *scale, int64_t s_scale_b,
+                               const void *shift, int64_t s_shift_b, float eps, int dtype, uint32_t flags,
+                               void *stream) {
+    adaln_status st =
+        check_ln(out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps, dtype, flags);
+    if (st != ADALN_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
+    LnArgs a{out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps};
+    return finish_launch(
+        launch_ln_modulate(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+adaln_status adaln_can_qk_head_layernorm(const void *q_out, const void *q, int64_t rows_q, const void *k_out,
+                                         const void *k, int64_t rows_k, int64_t Dh, const void *wq,
+                                         const void *bq, const void *wk, const void *bk, float eps, int dtype,
+                                         uint32_t flags) {
+    return check_qk(q_out, q, rows_q, k_out, k, rows_k, Dh, wq, bq, wk, bk, eps, dtype, flags);
+}
+
+adaln_status adaln_qk_head_layernorm(void *q_out, const void *q, int64_t rows_q, void *k_out, const void *k,
+                                     int64_t rows_k, int64_t Dh, const void *wq, const void *bq,
+                                     const void *wk, const void *bk, float eps, int dtype, uint32_t flags,
+                                     void *stream) {
+    adaln_status st = check_qk(q_out, q, rows_q, k_out, k, rows_k, Dh, wq, bq, wk, bk, eps, dtype, flags);
+    if (st != ADALN_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
+    QkArgs a{q_out, q, rows_q, k_out, k, rows_k, Dh, wq, bq, wk, bk, eps};
+    return finish_launch(
+        launch_qk_head_layernorm(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+adaln_status adaln_can_residual_gate_add(const void *out, const void *x, const void *gate, int64_t s_gate_b,
+                                         const void *y, int64_t B, int64_t N, int64_t D, int dtype,
+                                         uint32_t flags) {
+    return check_gate(out, x, gate, s_gate_b, y, B, N, D, dtype, flags);
+}
+
+adaln_status adaln_residual_gate_add(void *out, const void *x, const void *gate, int64_t s_gate_b,
+                                     const void *y, int64_t B, int64_t N, int64_t D, int dtype,
+                                     uint32_t flags, void *stream) {
+    adaln_status st = check_gate(out, x, gate, s_gate_b, y, B, N, D, dtype, flags);
+    if (st != ADALN_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
+    GateArgs a{out, x, gate, s_gate_b, y, B, N, D};
+    return finish_launch(
+        launch_residual_gate_add(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+adaln_status adaln_can_bias_gelu_tanh(const void *out, const void *x, const void *bias, int64_t rows,
+                                      int64_t width, int dtype, uint32_t flags) {
+    return check_gelu(out, x, bias, rows, width, dtype, flags);
+}
+
+adaln_status adaln_bias_gelu_tanh(void *out, const void *x, const void *bias, int64_t rows, int64_t width,
+                                  int dtype, uint32_t flags, void *stream) {
+    adaln_status st = check_gelu(out, x, bias, rows, width, dtype, flags);
+    if (st != ADALN_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
+    const void *table = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_dev[dev].gelu) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            cudaError_t e = cudaStreamIsCapturing((cudaStream_t)stream, &cs);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (cs != cudaStreamCaptureStatusNone) {
+                snprintf(g_err, sizeof(g_err),
+                         "GELU tables not built on device %d: call adaln_init before stream capture", dev);
+                return ADALN_E_CUDA;
+            }
+            if ((st = build_tables_locked(dev)) != ADALN_OK) return st;
+        }
+        table = (const uint16_t *)g_dev[dev].gelu + (dtype == ADALN_FP16 ? 65536 : 0);
+    }
+    GeluArgs a{out, x, bias, rows, width, table};
+    return finish_launch(
+        launch_bias_gelu_tanh(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+}  // extern "C"

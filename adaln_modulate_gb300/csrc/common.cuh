@@ -1,0 +1,325 @@
+// Device helpers shared by the sm_103a kernels of the fused DiT chains.
+//
+// Every floating-point step of the fixed rounding DAG is written with an
+// explicit round-to-nearest operation (intrinsic or PTX), so nvcc never
+// contracts a multiply and an add into an FMA or reassociates anything.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace adaln {
+
+enum class DT : int { BF16 = 0, FP16 = 1 };
+
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// ---------------------------------------------------------------- PDL
+
+// With ADALN_FLAG_PDL the kernel is launched with programmatic stream
+// serialisation; it must not read inputs before the preceding grid has
+// completed.  Without the launch attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------- 16-bit storage <-> f32
+
+// Element 0 of a packed pair sits in the low 16 bits.
+template <DT T> __device__ __forceinline__ float lo_f32(uint32_t p);
+template <DT T> __device__ __forceinline__ float hi_f32(uint32_t p);
+template <> __device__ __forceinline__ float lo_f32<DT::BF16>(uint32_t p) { return __uint_as_float(p << 16); }
+template <> __device__ __forceinline__ float hi_f32<DT::BF16>(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
+template <> __device__ __forceinline__ float lo_f32<DT::FP16>(uint32_t p) {
+    return __half2float(__ushort_as_half((unsigned short)(p & 0xffffu)));
+}
+template <> __device__ __forceinline__ float hi_f32<DT::FP16>(uint32_t p) {
+    return __half2float(__ushort_as_half((unsigned short)(p >> 16)));
+}
+template <DT T> __device__ __forceinline__ float h_f32(uint16_t h) { return lo_f32<T>((uint32_t)h); }
+
+// The same conversions through different instructions.  A kernel that
+// converts the same packed registers twice (statistics pass, then output
+// pass) uses these in the second pass, so that the compiler recomputes the
+// values instead of keeping every converted float alive in registers.
+template <DT T> __device__ __forceinline__ void unpack_again(uint32_t p, float &lo, float &hi);
+template <> __device__ __forceinline__ void unpack_again<DT::BF16>(uint32_t p, float &lo, float &hi) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, 0, 0x1044;" : "=r"(a) : "r"(p));
+    asm("prmt.b32 %0, %1, 0, 0x3244;" : "=r"(b) : "r"(p));
+    lo = __uint_as_float(a);
+    hi = __uint_as_float(b);
+}
+template <> __device__ __forceinline__ void unpack_again<DT::FP16>(uint32_t p, float &lo, float &hi) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, 0, 0x4410;" : "=r"(a) : "r"(p));
+    asm("prmt.b32 %0, %1, 0, 0x4432;" : "=r"(b) : "r"(p));
+    asm("{ .reg .b16 h; cvt.u16.u32 h, %1; cvt.f32.f16 %0, h; }" : "=f"(lo) : "r"(a));
+    asm("{ .reg .b16 h; cvt.u16.u32 h, %1; cvt.f32.f16 %0, h; }" : "=f"(hi) : "r"(b));
+}
+
+// round-to-nearest-even pack of two binary32 values: lo -> bits 0..15
+template <DT T> __device__ __forceinline__ uint32_t pack_rn(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack_rn<DT::BF16>(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+template <> __device__ __forceinline__ uint32_t pack_rn<DT::FP16>(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+template <DT T> __device__ __forceinline__ uint16_t to16_rn(float v) {
+    return (uint16_t)(pack_rn<T>(v, 0.0f) & 0xffffu);
+}
+
+// Packed 16-bit arithmetic, each lane rounded once to the storage type.
+// For one add or one multiply of two storage values this equals binary32
+// arithmetic followed by one storage rounding: binary32 carries at least
+// 2p+2 significand bits for p = 8 (bf16) and p = 11 (fp16), so the double
+// rounding is innocuous (Figueroa, "When is double rounding innocuous?",
+// SIGNUM 1995).
+template <DT T> __device__ __forceinline__ uint32_t add16x2(uint32_t a, uint32_t b);
+template <DT T> __device__ __forceinline__ uint32_t mul16x2(uint32_t a, uint32_t b);
+template <> __device__ __forceinline__ uint32_t add16x2<DT::BF16>(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <> __device__ __forceinline__ uint32_t mul16x2<DT::BF16>(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <> __device__ __forceinline__ uint32_t add16x2<DT::FP16>(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <> __device__ __forceinline__ uint32_t mul16x2<DT::FP16>(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// 1.0 in both lanes
+template <DT T> __device__ __forceinline__ uint32_t one16x2() {
+    return T == DT::BF16 ? 0x3f803f80u : 0x3c003c00u;
+}
+
+// ------------------------------------------------------ packed binary32
+
+typedef unsigned long long f2_t;  // two binary32 lanes: x in bits 0..31
+
+__device__ __forceinline__ f2_t f2(float x, float y) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f2_t v, float &x, float &y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
+    f2_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+    f2_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+    f2_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// ------------------------------------------------ global memory access
+
+// Streaming (read-once) loads of 8/16/32 bytes, not allocated in L1.
+__device__ __forceinline__ void ld_stream8(uint32_t *r, const void *p) {
+    asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream16(uint32_t *r, const void *p) {
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream32(uint32_t *r, const void *p) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]),
+                   "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]) : "l"(p));
+}
+// Loads of small rows re-read by many warps (scale / shift / gate / bias).
+__device__ __forceinline__ void ld_keep8(uint32_t *r, const void *p) {
+    asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "l"(p));
+}
+__device__ __forceinline__ void ld_keep16(uint32_t *r, const void *p) {
+    asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "l"(p));
+}
+__device__ __forceinline__ void ld_keep32(uint32_t *r, const void *p) {
+    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]),
+                   "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]) : "l"(p));
+}
+__device__ __forceinline__ void st8(void *p, const uint32_t *r) {
+    asm volatile("st.global.v2.b32 [%0], {%1, %2};" :: "l"(p), "r"(r[0]), "r"(r[1]) : "memory");
+}
+__device__ __forceinline__ void st16(void *p, const uint32_t *r) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]) : "memory");
+}
+__device__ __forceinline__ void st32(void *p, const uint32_t *r) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
+                    "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]) : "memory");
+}
+
+// 16 consecutive storage elements (32 bytes) moved with VEC-byte accesses;
+// the caller guarantees VEC-byte alignment.
+template <int VEC> __device__ __forceinline__ void ld16el_stream(uint32_t *r, const uint16_t *p) {
+    if constexpr (VEC == 32) {
+        ld_stream32(r, p);
+    } else if constexpr (VEC == 16) {
+        ld_stream16(r, p);
+        ld_stream16(r + 4, p + 8);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ld_stream8(r + 2 * k, p + 4 * k);
+    }
+}
+template <int VEC> __device__ __forceinline__ void ld16el_keep(uint32_t *r, const uint16_t *p) {
+    if constexpr (VEC == 32) {
+        ld_keep32(r, p);
+    } else if constexpr (VEC == 16) {
+        ld_keep16(r, p);
+        ld_keep16(r + 4, p + 8);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ld_keep8(r + 2 * k, p + 4 * k);
+    }
+}
+template <int VEC> __device__ __forceinline__ void st16el(uint16_t *p, const uint32_t *r) {
+    if constexpr (VEC == 32) {
+        st32(p, r);
+    } else if constexpr (VEC == 16) {
+        st16(p, r);
+        st16(p + 8, r + 4);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) st8(p + 4 * k, r + 2 * k);
+    }
+}
+
+// ------------------------------------------- Welford / Chan statistics
+
+// 1/n rounded to nearest binary32, as a compile-time constant: the
+// division is evaluated by the compiler front end in IEEE binary32.
+template <int N> struct Rcp {
+    static constexpr float value = 1.0f / static_cast<float>(N);
+};
+template <int E> __device__ __forceinline__ constexpr float rcp_const() { return Rcp<E>::value; }
+
+struct Stat {
+    float mean, m2, cnt;
+};
+
+// Chan's pairwise combine of the lower lane's state a and the upper lane's
+// state b: n = na + nb, coef = nb / n (0 when n == 0), delta = mb - ma,
+// mean = fma(delta, coef, ma), m2 = fma(delta^2 * na, coef, m2a + m2b).
+__device__ __forceinline__ Stat chan(const Stat &a, const Stat &b) {
+    Stat o;
+    float n = __fadd_rn(a.cnt, b.cnt);
+    float coef = (n == 0.0f) ? 0.0f : __fdiv_rn(b.cnt, n);
+    float delta = __fsub_rn(b.mean, a.mean);
+    o.mean = __fmaf_rn(delta, coef, a.mean);
+    float dda = __fmul_rn(__fmul_rn(delta, delta), a.cnt);
+    o.m2 = __fmaf_rn(dda, coef, __fadd_rn(a.m2, b.m2));
+    o.cnt = n;
+    return o;
+}
+
+// The same combine for a pair of independent rows sharing counts (the
+// coefficient is computed once).
+__device__ __forceinline__ void chan2(f2_t &ma, f2_t &qa, float na, f2_t mb, f2_t qb, float nb,
+                                      float &n_out) {
+    float n = __fadd_rn(na, nb);
+    float coef = (n == 0.0f) ? 0.0f : __fdiv_rn(nb, n);
+    f2_t delta = f2_sub(mb, ma);
+    f2_t c2 = f2(coef, coef);
+    f2_t na2 = f2(na, na);
+    ma = f2_fma(delta, c2, ma);
+    f2_t dda = f2_mul(f2_mul(delta, delta), na2);
+    float q0, q1, r0, r1;
+    f2_split(qa, q0, q1);
+    f2_split(qb, r0, r1);
+    f2_t qs = f2(__fadd_rn(q0, r0), __fadd_rn(q1, r1));
+    qa = f2_fma(dda, c2, qs);
+    n_out = n;
+}
+
+// Butterfly stage over a warp lane bit: both partners end with
+// chan(lower, upper).
+__device__ __forceinline__ Stat shfl_stage(const Stat &s, int xor_mask, unsigned mask = 0xffffffffu) {
+    Stat p;
+    p.mean = __shfl_xor_sync(mask, s.mean, xor_mask);
+    p.m2 = __shfl_xor_sync(mask, s.m2, xor_mask);
+    p.cnt = __shfl_xor_sync(mask, s.cnt, xor_mask);
+    const bool lower = (threadIdx.x & xor_mask) == 0;
+    return lower ? chan(s, p) : chan(p, s);
+}
+
+// ----------------------------------------------- correctly rounded rsqrt
+
+// Sign of (m^2 * x - 1) for the midpoint m = (a + nextup(a)) / 2 of a
+// positive normal binary32 a and a positive finite x, exactly, in integers:
+// m = (2A + 1) * 2^(ea - 1) with A the 24-bit significand of a.
+__device__ __forceinline__ int mid_sq_x_sign(float a, float x) {
+    uint32_t ua = __float_as_uint(a), ux = __float_as_uint(x);
+    int ea = (int)(ua >> 23) - 150;
+    uint64_t A = (ua & 0x7fffffu) | 0x800000u;
+    uint32_t Ex = ux >> 23;
+    uint64_t X = Ex ? ((ux & 0x7fffffu) | 0x800000u) : (ux & 0x7fffffu);
+    int ex = Ex ? (int)Ex - 150 : -149;
+    uint64_t S = 2 * A + 1;                 // < 2^25
+    uint64_t S2 = S * S;                    // < 2^50
+    uint64_t lo = S2 * X, hi = __umul64hi(S2, X);
+    int k = 2 * (ea - 1) + ex;              // m^2 x = (hi:lo) * 2^k
+    if (k >= 0) return 1;                   // (hi:lo) >= 1
+    int K = -k;                             // compare (hi:lo) with 2^K
+    if (K >= 128) return -1;
+    if (K >= 64) {
+        uint64_t t = 1ull << (K - 64);
+        if (hi != t) return hi > t ? 1 : -1;
+        return lo ? 1 : 0;
+    }
+    if (hi) return 1;
+    uint64_t t = 1ull << K;
+    return lo > t ? 1 : (lo < t ? -1 : 0);
+}
+
+// 1/sqrt(x) rounded to nearest binary32 for x > 0 (x = +0 -> +inf,
+// x = inf -> 0, x < 0 or NaN -> NaN).  The hardware-backed candidate is
+// checked against both rounding boundaries exactly and moved by one ulp if
+// it is on the wrong side (no exact ties exist).
+__device__ __forceinline__ float rsqrt_cr(float x) {
+    if (!(x > 0.0f) || isinf(x)) return __frsqrt_rn(x);
+    float r = __frsqrt_rn(x);
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        if (mid_sq_x_sign(r, x) <= 0) {
+            r = __uint_as_float(__float_as_uint(r) + 1u);   // 1/sqrt(x) above the upper midpoint
+        } else {
+            float dn = __uint_as_float(__float_as_uint(r) - 1u);
+            if (mid_sq_x_sign(dn, x) >= 0) r = dn;        // below the lower midpoint
+        }
+    }
+    return r;
+}
+
+}  // namespace adaln

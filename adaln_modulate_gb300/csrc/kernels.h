@@ -1,0 +1,97 @@
+// Host-side launchers of the sm_103a kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace adaln {
+
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    int max_smem_optin = 0;
+    int l2_bytes = 0;
+};
+
+struct LnArgs {
+    void *out;
+    const void *x;
+    int64_t B, N, D, sxB, sxN, sxD;
+    const void *scale;
+    int64_t s_scale_b;
+    const void *shift;
+    int64_t s_shift_b;
+    float eps;
+};
+
+struct QkArgs {
+    void *q_out;
+    const void *q;
+    int64_t rows_q;
+    void *k_out;
+    const void *k;
+    int64_t rows_k;
+    int64_t Dh;
+    const void *wq, *bq, *wk, *bk;
+    float eps;
+};
+
+struct GateArgs {
+    void *out;
+    const void *x;
+    const void *gate;
+    int64_t s_gate_b;
+    const void *y;
+    int64_t B, N, D;
+};
+
+struct GeluArgs {
+    void *out;
+    const void *x;
+    const void *bias;
+    int64_t rows, width;
+    const void *table;  // 65536 storage values of the dtype
+};
+
+// Which ln_modulate kernel a call takes (exposed for tests and the bench).
+enum LnPath : int { LN_PATH_ROWS = 0, LN_PATH_TOKENS = 1, LN_PATH_GENERIC = 2 };
+int ln_modulate_path(const LnArgs &a);
+
+cudaError_t launch_ln_modulate(const LnArgs &a, int dtype, bool pdl, cudaStream_t s,
+                               const DeviceInfo &dev);
+cudaError_t launch_qk_head_layernorm(const QkArgs &a, int dtype, bool pdl, cudaStream_t s,
+                                     const DeviceInfo &dev);
+cudaError_t launch_residual_gate_add(const GateArgs &a, int dtype, bool pdl, cudaStream_t s,
+                                     const DeviceInfo &dev);
+cudaError_t launch_bias_gelu_tanh(const GeluArgs &a, int dtype, bool pdl, cudaStream_t s,
+                                  const DeviceInfo &dev);
+cudaError_t launch_gelu_table_init(void *table, int dtype, cudaStream_t s);
+
+// cudaLaunchKernelEx with the optional programmatic-dependent-launch attribute
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Resident blocks per SM of a kernel at a block size / dynamic smem, cached
+// per (kernel, block size, smem); every device this library drives is the
+// same model.
+int blocks_per_sm_cached(const void *kernel, int threads, size_t smem);
+
+template <typename K>
+int blocks_per_sm(K kernel, int threads, size_t smem) {
+    return blocks_per_sm_cached(reinterpret_cast<const void *>(kernel), threads, smem);
+}
+
+}  // namespace adaln

@@ -1,0 +1,10 @@
+// ln_modulate contiguous-rows kernel, fp16 storage.
+#include "ln_rows.cuh"
+
+namespace adaln {
+
+cudaError_t ln_rows_fp16(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    return rows_vec<DT::FP16>(a, pdl, s, dev);
+}
+
+}  // namespace adaln

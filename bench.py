@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused DiT chains on GB300 (one JSON line on stdout).
+
+Headline: fused LayerNorm + adaLN modulate on the Sana block shape
+(2, 1024, 2240) bf16, x given as the transposed view of a contiguous
+(2, 2240, 1024) tensor, adaLN table (2, 6, 2240) with scale = chunk 1 and
+shift = chunk 0, eps = 1e-6.  One step = one call of the op on that input.
+value = algorithmic bytes (x read once, out written once, scale / shift rows
+read once) / mean device time per call, in GB/s.
+
+Timing: W untimed warm-up calls, then K timed calls.  Before every call L2
+is flushed (a 256 MiB buffer is written, then another is read, so no dirty
+flush lines are left to write back during the call) and each call is
+bracketed by CUDA events on the launching stream.  Clocks and throttle
+reasons are sampled with nvidia-smi during the timed region.
+
+Also reported: e2e (the same metric with the inputs copied host -> device
+from pinned memory and the output copied back inside every timed step), the
+roofline of the timed kernel against the measured HBM copy bandwidth, the
+CPU oracle timed on the host (cpu_baseline), and per-workload numbers of all
+four chains next to a same-byte device-to-device copy (per_config).
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+                  [--quick] [--no-per-config] [--no-cpu]
+Under torchrun (N > 1) every rank runs its own replica (no data exchange);
+value is the sum over ranks, time the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused LN+modulate GB/s and µs/call at (2,1024,2240) bf16; % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------ utilities
+
+def ln_bytes(B, N, D):
+    return 2 * B * N * D * 2 + 2 * B * D * 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+TOKENS_SOURCES = ["adaln_modulate_gb300/csrc/ln_tokens.cu", "adaln_modulate_gb300/csrc/ln_common.cuh",
+                  "adaln_modulate_gb300/csrc/common.cuh"]
+
+
+def profiled_traffic(summary_name, sources):
+    """DRAM bytes per launch recorded in a committed ncu summary, if the
+    kernel sources still hash to what was profiled; else None."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m or not t or m.group(1) != kernel_source_hash(sources):
+        return None
+    return int(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            except Exception:
+                ts = None
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if ts is not None and self.t0 is not None
+                  and self.t0 - 0.06 <= ts <= (self.t1 or ts) + 0.06]
+        use = inside if inside else [p for _, p in rows]
+        sm = [float(p[2]) for p in use if re.match(r"^[0-9.]+$", p[2])]
+        smax = [float(p[3]) for p in use if re.match(r"^[0-9.]+$", p[3])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if p[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(use),
+                "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------ workloads
+
+def torch_bits(bits, dtype, dev):
+    import numpy as np
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+        torch.bfloat16 if dtype == "bf16" else torch.float16)
+    return t.to(dev)
+
+
+def make_workloads(dev, which):
+    """name -> (callable issuing one op, algorithmic bytes, description)."""
+    import torch
+
+    import adaln_modulate_gb300 as ad
+    import synth
+
+    out = {}
+    if "sana" in which or "sana_nmod2" in which:
+        for nmod in ([6] if "sana" in which else []) + ([2] if "sana_nmod2" in which else []):
+            w = synth.ln_sana(nmod=nmod)
+            B, N, D = 2, 1024, 2240
+            xb = torch_bits(w.tensors["x"].draw(), "bf16", dev)
+            tb = torch_bits(w.tensors["table"].draw(), "bf16", dev)
+            x = xb.permute(0, 2, 1)
+            sc, sh = tb[:, 1:2], tb[:, 0:1]
+            o = torch.empty((B, N, D), dtype=torch.bfloat16, device=dev)
+            out["sana" if nmod == 6 else "sana_nmod2"] = (
+                lambda x=x, sc=sc, sh=sh, o=o: ad.ln_modulate(x, sc, sh, 1e-6, out=o),
+                ln_bytes(B, N, D), w.name)
+    if "tiny" in which:
+        w = synth.ln_tiny()
+        x, sc, sh = (torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift"))
+        o = torch.empty_like(x)
+        out["tiny"] = (lambda: ad.ln_modulate(x, sc, sh, 1e-6, out=o), ln_bytes(1, 64, 512), w.name)
+    if "glm_ln" in which or "glm_gate" in which:
+        w = synth.ln_glm()
+        x, sc, sh = (torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift"))
+        o = torch.empty_like(x)
+        if "glm_ln" in which:
+            out["glm_ln"] = (lambda: ad.ln_modulate(x, sc, sh, 1e-5, out=o), ln_bytes(1, 4096, 4096),
+                             w.name)
+        if "glm_gate" in which:
+            wg = synth.gate_add_glm()
+            y = torch_bits(wg.tensors["y"].draw(), "bf16", dev)
+            g = torch_bits(wg.tensors["gate"].draw(), "bf16", dev)
+            o2 = torch.empty_like(x)
+            out["glm_gate"] = (lambda: ad.residual_gate_add(x, g, y, out=o2),
+                               3 * 4096 * 4096 * 2 + 4096 * 2, wg.name)
+    if "qk" in which:
+        w = synth.qk_glm()
+        q, k = (torch_bits(w.tensors[n].draw(), "bf16", dev) for n in ("q", "k"))
+        ws = [torch_bits(w.tensors[n].draw(), "bf16", dev) for n in ("wq", "bq", "wk", "bk")]
+        qo, ko = torch.empty_like(q), torch.empty_like(k)
+        rows = 4360 * 32
+        out["qk"] = (lambda: ad.qk_head_layernorm(q, k, *ws, 1e-6, q_out=qo, k_out=ko),
+                     2 * 2 * rows * 128 * 2 + 4 * 128 * 2, w.name)
+    for dt in ("bf16", "fp16"):
+        key = f"gelu_{dt}"
+        if key in which:
+            w = synth.gelu_wan(dt)
+            x = torch_bits(w.tensors["x"].draw(dt), dt, dev)
+            b = torch_bits(w.tensors["bias"].draw(dt), dt, dev)
+            o = torch.empty_like(x)
+            out[key] = (lambda x=x, b=b, o=o: ad.bias_gelu_tanh(x, b, out=o),
+                        2 * 32760 * 13824 * 2 + 13824 * 2, w.name)
+    return out
+
+
+# ------------------------------------------------------------ timing
+
+class Flusher:
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.fill_(1.0)
+        torch.sum(self.r, out=self.sink)
+
+
+def time_calls(fn, steps, warmup, flush, on_begin=None, on_end=None):
+    """Per-call device time (ms) of fn, each call after an L2 flush."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if on_begin:
+        on_begin()
+    for i in range(steps):
+        flush()
+        starts[i].record()
+        fn()
+        ends[i].record()
+    torch.cuda.synchronize()
+    if on_end:
+        on_end()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def e2e_sana(dev, steps, warmup):
+    """Host-to-host: pinned inputs copied in, op, output copied back."""
+    import torch
+
+    import adaln_modulate_gb300 as ad
+    import synth
+    w = synth.ln_sana()
+    B, N, D = 2, 1024, 2240
+    import numpy as np
+    hx = torch.from_numpy(w.tensors["x"].draw().view(np.int16)).view(torch.bfloat16).pin_memory()
+    ht = torch.from_numpy(w.tensors["table"].draw().view(np.int16)).view(torch.bfloat16).pin_memory()
+    ho = torch.empty((B, N, D), dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty_like(hx, device=dev)
+    dt = torch.empty_like(ht, device=dev)
+    do = torch.empty((B, N, D), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        dt.copy_(ht, non_blocking=True)
+        ad.ln_modulate(dx.permute(0, 2, 1), dt[:, 1:2], dt[:, 0:1], 1e-6, out=do)
+        ho.copy_(do, non_blocking=True)
+
+    times = time_calls(step, steps, warmup, lambda: None)
+    h2d = hx.numel() * 2 + ht.numel() * 2
+    d2h = ho.numel() * 2
+    return statistics.mean(times), h2d, d2h
+
+
+def time_copy(dev, nbytes, steps, warmup, flush):
+    import torch
+    n = nbytes // 2 // 2  # read + write == nbytes
+    a = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    return time_calls(lambda: b.copy_(a), steps, warmup, flush)
+
+
+# ------------------------------------------------------------ CPU baseline
+
+def cpu_baseline(budget_s=10.0):
+    """The oracle on the headline workload, on all host cores."""
+    import oracle
+    import synth
+    w = synth.ln_sana()
+    B, N, D = 2, 1024, 2240
+    x, table = w.tensors["x"].draw(), w.tensors["table"].draw()
+    cores = os.cpu_count() or 1
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.ln_modulate(x, B, N, D, (D * N, 1, N), table, D, 6 * D, table, 0, 6 * D, 1e-6,
+                           threads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    per = el / reps
+    return {"value": round(ln_bytes(B, N, D) / per / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "seconds_per_call": round(per, 5),
+            "sample": f"the full headline workload (2048 rows x 2240), {reps} calls, "
+                      f"{el:.1f} s, rows split over {cores} threads"}
+
+
+# ------------------------------------------------------------ arms
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    w = synth.ln_sana()
+    B, N, D = 2, 1024, 2240
+    x, table = w.tensors["x"].draw(), w.tensors["table"].draw()
+    cores = os.cpu_count() or 1
+    call = lambda: oracle.ln_modulate(x, B, N, D, (D * N, 1, N), table, D, 6 * D, table, 0, 6 * D,
+                                      1e-6, threads=cores)
+    steps = max(1, min(args.steps, 100))
+    warm = max(0, min(args.warmup, 3))
+    for _ in range(warm):
+        call()
+    t = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        call()
+        t.append(time.perf_counter() - t0)
+    per = statistics.mean(t)
+    value = ln_bytes(B, N, D) / per / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": round(per * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "N": N, "D": D, "layout": "transposed view",
+                       "nmod": 6, "eps": 1e-6, "runs_on": "host CPU (the oracle)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": f"the full workload per step, {steps} steps"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    import adaln_modulate_gb300 as ad
+    ad.init(local)
+    flush = Flusher(dev)
+
+    main = make_workloads(dev, ["sana"])["sana"]
+    fn, nbytes, wname = main
+    sampler = ClockSampler(local)
+    sampler.start()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+
+    barrier()
+    times = time_calls(fn, args.steps, args.warmup, flush, on_begin=sampler.mark_begin,
+                       on_end=sampler.mark_end)
+    barrier()
+    clocks = sampler.stop()
+    mean_ms = statistics.mean(times)
+    if ws > 1:
+        t = torch.tensor([mean_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    value = ws * nbytes / (mean_ms * 1e-3) / 1e9
+    per_gpu = nbytes / (mean_ms * 1e-3) / 1e9
+    hbm, src = peaks()
+    traffic = profiled_traffic("ln_modulate_tokens_sana.md", TOKENS_SOURCES)
+    roof = {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(per_gpu / hbm, 4), "traffic": traffic,
+            "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs, burst copy)" if src == "measured"
+            else "fallback 6.8 TB/s", "kernel": "ln_tokens_kernel<bf16, 5>",
+            "algorithmic_bytes_per_launch": nbytes}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
+            "us_per_call": round(mean_ms * 1e3, 3),
+            "us_per_call_p10_p90": [round(1e3 * sorted(times)[len(times) // 10], 3),
+                                    round(1e3 * sorted(times)[(9 * len(times)) // 10], 3)],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wname, "B": 2, "N": 1024, "D": 2240,
+                       "layout": "x = transposed view of contiguous (2, 2240, 1024)",
+                       "nmod": 6, "scale_chunk": 1, "shift_chunk": 0, "eps": 1e-6,
+                       "l2": "flushed before every timed call (256 MiB written, then 256 MiB read)",
+                       "parallelism": f"replicas x{ws} (rows independent, no exchange)"},
+            "roofline": roof, "gpu_launches": args.steps, "clocks": clocks}
+
+    if rank == 0 and not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_sana(dev, min(args.steps, 300), min(args.warmup, 10))
+        line["e2e"] = {"value": round(ws * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(e2e_ms, 4),
+                       "how": "pinned host x and adaLN table copied in, op, output copied out, "
+                              "per step, CUDA events around the whole step"}
+    if rank == 0 and not args.no_per_config:
+        names = ["tiny", "sana", "sana_nmod2", "glm_ln", "glm_gate", "qk", "gelu_bf16", "gelu_fp16"]
+        wl = make_workloads(dev, names)
+        per = {}
+        steps = max(10, min(args.steps, 200))
+        for name in names:
+            f, nb, desc = wl[name]
+            t = time_calls(f, steps, 5, flush)
+            tc = time_copy(dev, nb, steps, 5, flush)
+            us, usc = statistics.mean(t) * 1e3, statistics.mean(tc) * 1e3
+            per[name] = {"workload": desc, "us_per_call": round(us, 3),
+                         "gbs": round(nb / (us * 1e-6) / 1e9, 1),
+                         "frac_of_hbm_peak": round(nb / (us * 1e-6) / 1e9 / hbm, 4),
+                         "algorithmic_bytes": nb, "copy_same_bytes_us": round(usc, 3),
+                         "copy_same_bytes_gbs": round(nb / (usc * 1e-6) / 1e9, 1)}
+            del f
+        line["per_config"] = per
+        line["gpu_launches"] = args.steps  # the headline's timed region; per_config is separate
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-per-config", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--quick", action="store_true", help="headline only (for profiler runs)")
+    args = p.parse_args()
+    if args.quick:
+        args.no_per_config = args.no_cpu = args.no_e2e = True
+    if args.warmup < 3 and not args.quick:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+/*
+ * adaln.h -- C ABI of the fused non-GEMM chains of a diffusion-transformer
+ * block, for NVIDIA GB300 (sm_103a).
+ *
+ * Four operations, each the fused form of an eager PyTorch chain described
+ * on the SGLang Diffusion "Fused Kernels" page and its pull-request pages:
+ *
+ *   adaln_ln_modulate          LayerNorm (no affine) + adaLN modulate
+ *   adaln_qk_head_layernorm    per-head LayerNorm with affine on q and k
+ *   adaln_residual_gate_add    x + gate * y
+ *   adaln_bias_gelu_tanh       tanh-GELU of (x + bias)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are caller-owned device buffers of 16-bit storage values
+ *    (bf16 or fp16, `adaln_dtype`); sizes and strides are in ELEMENTS.
+ *  - Every operation is asynchronous on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream) and never synchronises the host.
+ *  - Arguments are validated entirely on the host before anything is
+ *    launched.  On failure the call returns a non-zero `adaln_status`,
+ *    launches nothing and leaves every buffer untouched.  A CUDA error at
+ *    launch returns ADALN_E_CUDA (the CUDA error string is available from
+ *    adaln_last_cuda_error()).  No C++ exception crosses this interface.
+ *  - Arithmetic: binary32 with the storage rounding points of the eager
+ *    chain; results are bit-identical for a given input on every launch
+ *    geometry (a fixed reduction order, described per operation).
+ *    NaN results are NaN; their payload bits are not specified.
+ *  - adaln_can_* take the same arguments as the operation (minus the
+ *    stream), run no CUDA call and return what the operation would return
+ *    from validation (ADALN_OK when it would launch).
+ *  - Thread safety: calls may be made from several host threads.
+ *  - Memory: no call allocates device memory, except the one-time
+ *    per-device GELU tables of adaln_bias_gelu_tanh (adaln_init).
+ */
+#ifndef ADALN_H
+#define ADALN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum adaln_status {
+    ADALN_OK = 0,
+    ADALN_E_NULL = 1,    /* a required pointer is NULL */
+    ADALN_E_DTYPE = 2,   /* dtype is not ADALN_BF16 / ADALN_FP16 */
+    ADALN_E_SHAPE = 3,   /* a size is out of range (see each operation) */
+    ADALN_E_ALIGN = 4,   /* a pointer is not aligned to the element size */
+    ADALN_E_STRIDE = 5,  /* a stride is negative or makes rows overlap */
+    ADALN_E_VALUE = 6,   /* eps negative or not finite, or unknown flag bits */
+    ADALN_E_OVERLAP = 7, /* an output overlaps an input in a way not allowed */
+    ADALN_E_CUDA = 8     /* a CUDA runtime call failed */
+} adaln_status;
+
+typedef enum adaln_dtype {
+    ADALN_BF16 = 0,
+    ADALN_FP16 = 1
+} adaln_dtype;
+
+/* flags */
+#define ADALN_FLAG_PDL 1u /* launch with programmatic dependent launch: the
+                             kernel may start while the previous kernel on
+                             the stream finishes, and waits for it before
+                             reading any input */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *adaln_status_str(int status);
+
+/* Text of the last CUDA error seen by this library in the calling host
+ * thread ("" if none). */
+const char *adaln_last_cuda_error(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int adaln_version(void);
+
+/* One-time per-device set-up: queries the device and builds the two
+ * 65536-entry GELU tables of adaln_bias_gelu_tanh (2 x 128 KiB of device
+ * memory, owned by the library).  Synchronous.  Calling it is optional:
+ * the first adaln_bias_gelu_tanh on a device does it too, which is not
+ * allowed while the stream is being captured into a CUDA graph, so call
+ * adaln_init first when capturing.  Idempotent. */
+adaln_status adaln_init(int device);
+
+/* Frees what adaln_init allocated, on every device.  Call only when no
+ * operation of this library is in flight. */
+adaln_status adaln_shutdown(void);
+
+/* ------------------------------------------------------------------------
+ * adaln_ln_modulate
+ *   out[b, n, :] = LN(x[b, n, :]) * (1 + scale[b, :]) + shift[b, :]
+ *
+ * The fused "layernorm_modulate" of the Fused Kernels page (Normalization
+ * table: affine-free LayerNorm + adaLN modulate, bit-exact contract), with
+ * the tail-chunk generalisation to D % 4 == 0 of PR #34015 and the
+ * per-sample (B, 1, D) scale / shift rows of PR #34008.
+ *
+ *   x      (B, N, D) with element strides (sxB, sxN, sxD): element (b,n,d)
+ *          at x[b*sxB + n*sxN + d*sxD].  Contiguous (sxD == 1) and the
+ *          transposed view of a contiguous (B, D, N) tensor (sxN == 1, as
+ *          in Sana) have dedicated kernels; any other non-negative strides
+ *          are accepted and take a slower general kernel.
+ *   out    (B, N, D) contiguous.  May equal x only when x is contiguous
+ *          (sxD == 1, sxN == D, sxB == N*D); otherwise must not overlap x.
+ *   scale, shift  row b starts at scale + b*s_scale_b (resp. shift +
+ *          b*s_shift_b) and is contiguous over D: the (B, 1, D) chunk views
+ *          of an adaLN table (B, nmod, D) are (table + c*D, nmod*D).
+ *   eps    finite, >= 0 (used as a binary32 value).
+ *   Limits: B, N >= 1; 4 <= D <= 65536, D % 4 == 0.
+ *
+ * Numerics (fixed, independent of the launch geometry): 128 logical lanes;
+ * lane l accumulates vec4 chunks j = i*128 + l (j < D/4) with the serial
+ * Welford update mean' = fma(d, 1/(c+1), mean), m2' = fma(d, x - mean', m2)
+ * (IEEE division); lanes are merged by Chan's pairwise combine in the
+ * butterfly order 16, 8, 4, 2, 1, 64, 32; var = m2 / D; rstd = correctly
+ * rounded 1/sqrt(var + eps); per element y = round(rstd*(x - mean)),
+ * op = round(1 + scale), p = round(y*op), out = round(p + shift).
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_ln_modulate(void *out, const void *x, int64_t B, int64_t N, int64_t D,
+                               int64_t sxB, int64_t sxN, int64_t sxD,
+                               const void *scale, int64_t s_scale_b,
+                               const void *shift, int64_t s_shift_b,
+                               float eps, int dtype, uint32_t flags, void *stream);
+
+adaln_status adaln_can_ln_modulate(const void *out, const void *x, int64_t B, int64_t N,
+                                   int64_t D, int64_t sxB, int64_t sxN, int64_t sxD,
+                                   const void *scale, int64_t s_scale_b,
+                                   const void *shift, int64_t s_shift_b,
+                                   float eps, int dtype, uint32_t flags);
+
+/* Which kernel adaln_ln_modulate would launch for these arguments (no CUDA
+ * call): 0 = contiguous rows (sxD == 1, D <= 4096, 8-byte aligned rows),
+ * 1 = contiguous tokens (sxN == 1, the transposed view; D <= 6144, 16-byte
+ * aligned d-rows), 2 = general strides.  The numbers are identical on every
+ * path.  Returns the negative adaln_status if the arguments are invalid. */
+int adaln_ln_modulate_variant(const void *out, const void *x, int64_t B, int64_t N,
+                              int64_t D, int64_t sxB, int64_t sxN, int64_t sxD,
+                              const void *scale, int64_t s_scale_b,
+                              const void *shift, int64_t s_shift_b,
+                              float eps, int dtype, uint32_t flags);
+
+/* ------------------------------------------------------------------------
+ * adaln_qk_head_layernorm
+ *   q_out[r, :] = LN(q[r, :]) * wq + bq,  k_out[r, :] = LN(k[r, :]) * wk + bk
+ *
+ * The "qk_head_layernorm" of the Fused Kernels page (per-head LayerNorm on
+ * q / k, bit-exact) as used by GLM-Image (PR #34008): both tensors in ONE
+ * launch.  q is (rows_q, Dh), k is (rows_k, Dh), both contiguous (rows =
+ * B*N*H for a (B, N, H, Dh) tensor).  wq, bq, wk, bk are (Dh,) vectors
+ * (the same pointers may be passed for q and k).  Outputs are contiguous;
+ * q_out may equal q and k_out may equal k (in place); no other overlap.
+ * rows_q or rows_k may be 0 (that tensor is skipped; its pointers may be
+ * NULL), not both.
+ *   Limits: 4 <= Dh <= 128, Dh % 4 == 0; eps finite, >= 0.
+ * Numerics: as adaln_ln_modulate with 32 logical lanes (lane l holds
+ * elements 4l..4l+3; butterfly 16, 8, 4, 2, 1), then
+ * out = round(fma(w, rstd*(x - mean), b)) with one rounding.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_qk_head_layernorm(void *q_out, const void *q, int64_t rows_q,
+                                     void *k_out, const void *k, int64_t rows_k, int64_t Dh,
+                                     const void *wq, const void *bq,
+                                     const void *wk, const void *bk,
+                                     float eps, int dtype, uint32_t flags, void *stream);
+
+adaln_status adaln_can_qk_head_layernorm(const void *q_out, const void *q, int64_t rows_q,
+                                         const void *k_out, const void *k, int64_t rows_k,
+                                         int64_t Dh, const void *wq, const void *bq,
+                                         const void *wk, const void *bk,
+                                         float eps, int dtype, uint32_t flags);
+
+/* ------------------------------------------------------------------------
+ * adaln_residual_gate_add
+ *   out[b, n, d] = x[b, n, d] + gate[b, d] * y[b, n, d]
+ *
+ * The "residual_gate_add" of the Fused Kernels page (adaLN modulation and
+ * gating table: residual + gate * update, bit-exact), GLM-Image's ff-gate
+ * (PR #34008).  x, y, out contiguous (B, N, D); gate row b at
+ * gate + b*s_gate_b, contiguous over D (a (B, 1, D) tensor has
+ * s_gate_b = D).  out may equal x or y; no other overlap.
+ *   Limits: B, N >= 1; D >= 1.
+ * Numerics: out = round(x + round(gate * y)) (two storage roundings, no
+ * fused multiply-add).
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_residual_gate_add(void *out, const void *x, const void *gate,
+                                     int64_t s_gate_b, const void *y,
+                                     int64_t B, int64_t N, int64_t D,
+                                     int dtype, uint32_t flags, void *stream);
+
+adaln_status adaln_can_residual_gate_add(const void *out, const void *x, const void *gate,
+                                         int64_t s_gate_b, const void *y,
+                                         int64_t B, int64_t N, int64_t D,
+                                         int dtype, uint32_t flags);
+
+/* ------------------------------------------------------------------------
+ * adaln_bias_gelu_tanh
+ *   out[r, c] = gelu_tanh(round(x[r, c] + bias[c]))
+ *
+ * The bias + tanh-GELU epilogue of the Wan2.2 FFN (PR #37075, "功能与动机"
+ * and the bias_gelu_tanh kernel): fp32 add, rounded back to the storage
+ * type BEFORE the activation, then tanh-GELU, rounded again.  x, out
+ * contiguous (rows, width); bias (width,).  out may equal x.
+ *   Limits: rows >= 1; width >= 1.
+ * Numerics: gelu_tanh(v) is the binary32 value nearest to the exact
+ * 0.5*v*(1 + tanh(sqrt(2/pi)*(v + 0.044715*v^3))), then rounded to the
+ * storage type; it is read from a 65536-entry table per dtype (built once
+ * per device, see adaln_init), exact for every input.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_bias_gelu_tanh(void *out, const void *x, const void *bias,
+                                  int64_t rows, int64_t width,
+                                  int dtype, uint32_t flags, void *stream);
+
+adaln_status adaln_can_bias_gelu_tanh(const void *out, const void *x, const void *bias,
+                                      int64_t rows, int64_t width,
+                                      int dtype, uint32_t flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADALN_H */

@@ -1,0 +1,120 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/adaln.h declares, and validates arguments on the host (returning a
+status and launching nothing) before making any CUDA call."""
+import ctypes
+
+import pytest
+
+
+@pytest.fixture(scope="module")
+def ad():
+    import __graft_entry__
+    from adaln_modulate_gb300 import _build
+    _build.build()
+    import adaln_modulate_gb300
+    return adaln_modulate_gb300
+
+
+def test_every_declared_symbol_is_exported(ad):
+    names = ad.header_functions()
+    assert len(names) >= 14
+    lib = ctypes.CDLL(ad.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(ad.capi, n), n
+
+
+def test_status_strings(ad):
+    for code in range(9):
+        assert ad.capi.adaln_status_str(code).decode().startswith(ad.STATUS[code])
+    assert b"unknown" in ad.capi.adaln_status_str(99)
+    assert ad.capi.adaln_version() == 10000
+
+
+# Fake but aligned "device" addresses: validation never dereferences them.
+OUT, X, SC, SH = 0x10000000, 0x20000000, 0x30000000, 0x30100000
+
+
+def ln_can(ad, out=OUT, x=X, B=2, N=16, D=2240, strides=None, sc=SC, ssb=6 * 2240, sh=SH,
+           shb=6 * 2240, eps=1e-6, dtype=0, flags=0):
+    strides = strides or (N * D, D, 1)
+    return ad.capi.adaln_can_ln_modulate(out, x, B, N, D, *strides, sc, ssb, sh, shb, eps, dtype, flags)
+
+
+def test_ln_validation(ad):
+    assert ln_can(ad) == 0
+    assert ln_can(ad, dtype=2) == 2
+    assert ln_can(ad, x=None) == 1 and ln_can(ad, sc=None) == 1
+    for D in (0, 2, 6, 65540):
+        assert ln_can(ad, D=D) == 3, D
+    assert ln_can(ad, B=0) == 3 and ln_can(ad, N=0) == 3
+    assert ln_can(ad, strides=(16 * 2240, 2240, -1)) == 5
+    assert ln_can(ad, ssb=-1) == 5
+    assert ln_can(ad, eps=-1.0) == 6 and ln_can(ad, eps=float("inf")) == 6
+    assert ln_can(ad, eps=float("nan")) == 6
+    assert ln_can(ad, flags=2) == 6
+    assert ln_can(ad, x=X + 1) == 4
+    # out overlapping a non-contiguous x, or the scale rows, is refused
+    assert ln_can(ad, out=X, strides=(2240 * 16, 1, 16)) == 7
+    assert ln_can(ad, out=SC - 100) == 7
+    # in place on contiguous x is allowed
+    assert ln_can(ad, out=X) == 0
+
+
+def test_ln_invalid_call_returns_before_cuda(ad):
+    # status is returned from validation; no stream or device is touched
+    st = ad.capi.adaln_ln_modulate(OUT, X, 2, 16, 6, 16 * 6, 6, 1, SC, 6, SH, 6, 1e-6, 0, 0, None)
+    assert st == 3
+
+
+def test_ln_path_selection(ad):
+    v = ad.capi.adaln_ln_modulate_variant
+    # GLM contiguous rows
+    assert v(OUT, X, 1, 4096, 4096, 4096 * 4096, 4096, 1, SC, 4096, SH, 4096, 1e-5, 0, 0) == 0
+    # Sana transposed view of (2, 2240, 1024), nmod = 6 chunks
+    assert v(OUT, X, 2, 1024, 2240, 2240 * 1024, 1, 1024, SC + 2 * 2240, 6 * 2240, SC, 6 * 2240,
+             1e-6, 0, 0) == 1
+    # D too large for the register / shared-memory kernels, odd strides
+    assert v(OUT, X, 1, 8, 8192, 8 * 8192, 8192, 1, SC, 8192, SH, 8192, 1e-5, 0, 0) == 2
+    assert v(OUT, X, 1, 8, 512, 3 * 8 * 512, 3 * 512, 3, SC, 512, SH, 512, 1e-5, 0, 0) == 2
+    # misaligned row pitch for 8-byte accesses
+    assert v(OUT, X + 2, 1, 8, 512, 8 * 512, 512, 1, SC, 512, SH, 512, 1e-5, 0, 0) == 2
+    assert v(OUT, X, 1, 8, 6, 48, 6, 1, SC, 6, SH, 6, 1e-5, 0, 0) == -3
+
+
+def test_qk_validation(ad):
+    c = ad.capi.adaln_can_qk_head_layernorm
+    W = [0x40000000 + 0x1000 * i for i in range(4)]
+    ok = lambda **kw: c(kw.get("qo", OUT), kw.get("q", X), kw.get("rq", 100), kw.get("ko", OUT + 0x100000),
+                        kw.get("k", X + 0x100000), kw.get("rk", 100), kw.get("Dh", 128), *W,
+                        kw.get("eps", 1e-6), kw.get("dtype", 0), 0)
+    assert ok() == 0
+    assert ok(Dh=132) == 3 and ok(Dh=2) == 3 and ok(Dh=66) == 3
+    assert ok(rq=0, rk=0) == 3
+    assert ok(rq=0, q=None, qo=None) == 0
+    assert ok(q=None) == 1
+    assert ok(q=X + 2) == 4
+    assert ok(qo=X) == 0                      # in place
+    assert ok(qo=X + 64) == 7                 # partial overlap
+    assert ok(ko=OUT + 128) == 7              # outputs overlap each other
+    assert ok(dtype=5) == 2
+
+
+def test_gate_and_gelu_validation(ad):
+    g = ad.capi.adaln_can_residual_gate_add
+    assert g(OUT, X, SC, 4096, SH, 1, 4096, 4096, 0, 0) == 0
+    assert g(OUT, X, SC, 4096, SH, 1, 4096, 0, 0, 0) == 3
+    assert g(OUT, X, SC, -1, SH, 1, 4096, 4096, 0, 0) == 5
+    assert g(X, X, SC, 4096, SH, 1, 4096, 4096, 0, 0) == 0           # in place on x
+    assert g(X + 2, X, SC, 4096, SH, 1, 4096, 4096, 0, 0) == 7
+    assert g(OUT, X + 1, SC, 4096, SH, 1, 4096, 4096, 0, 0) == 4
+    b = ad.capi.adaln_can_bias_gelu_tanh
+    big_out, big_x = 1 << 40, 1 << 41          # 906 MB tensors far apart
+    assert b(big_out, big_x, SC, 32760, 13824, 0, 0) == 0
+    assert b(big_out, big_x, SC, 32760, 13824, 1, 0) == 0
+    assert b(OUT, X, SC, 32760, 13824, 0, 0) == 7     # out would run into x
+    assert b(OUT, X, SC, 0, 13824, 0, 0) == 3
+    assert b(OUT, X, None, 10, 10, 0, 0) == 1
+    assert b(OUT, X, OUT + 4, 10, 10, 0, 0) == 7
+    assert b(OUT, X, SC, 10, 10, 3, 0) == 2
