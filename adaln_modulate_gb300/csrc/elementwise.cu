@@ -219,11 +219,12 @@ static cudaError_t run_gelu(const GeluArgs &a, bool pdl, cudaStream_t s, const D
                         (const uint16_t *)a.table);
     } else {
         auto k = bias_gelu_kernel<T, EPT>;
-        static bool attr_set = false;
-        if (!attr_set) {
+        static bool attr_set[64] = {};  // per device
+        if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+        if (!attr_set[dev.device]) {
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGeluSmem);
             if (e != cudaSuccess) return e;
-            attr_set = true;
+            attr_set[dev.device] = true;
         }
         const int64_t nvec = n / EPT;
         const int64_t grid = imin64((nvec + kGeluThreads - 1) / kGeluThreads,

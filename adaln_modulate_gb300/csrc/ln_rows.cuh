@@ -120,17 +120,7 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t N, int D,
         f2_split(q23, st[2].m2, st[3].m2);
 #pragma unroll
         for (int s = 0; s < 4; ++s) st[s].cnt = cnt[s];
-#pragma unroll
-        for (int s = 0; s < 4; ++s) st[s] = shfl_stage(st[s], 4);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) st[s] = shfl_stage(st[s], 2);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) st[s] = shfl_stage(st[s], 1);
-        Stat a = chan(st[0], st[2]);
-        Stat c = chan(st[1], st[3]);
-        Stat f = chan(a, c);
-        f = shfl_stage(f, 16);
-        f = shfl_stage(f, 8);
+        const Stat f = fold128_k4(st);
         const float mean = f.mean;
         const float rstd = finish_rstd(f.m2, Df, eps);
 

@@ -6,9 +6,25 @@ namespace adaln {
 
 // ---------------------------------------------------------------------
 // tokens contiguous (transposed view): 8 tokens per CTA
+//
+// 512 threads; thread (l, p) is logical lane l = 8*warp + ((tid >> 2) & 7)
+// for the token pair p = tid & 3 (tokens 2p, 2p+1).  Data flow per tile:
+//   1. thread (l, p) copies the d-rows 4*(128*i + l) + p (8 tokens, 16 bytes
+//      each) into the tile with cp.async; the 4 threads of a lane sit in one
+//      warp, so a warp barrier makes a lane's 4 rows visible to all of them;
+//   2. pass 1: serial Welford of lane l for tokens 2p, 2p+1 (one f32x2 op
+//      covers both tokens), state to shared memory;
+//   3. warps 0..7 fold token t = warp over the 128 lane states (4 lanes per
+//      thread, the same butterfly as the contiguous-rows kernel) and write
+//      mean / rstd of the token;
+//   4. pass 2: thread (l, p) normalises its rows for its two tokens, applies
+//      the modulate and stores 4 consecutive d of each token (8 bytes).
+// Shared-memory reads of a warp cover 128 contiguous bytes (8 lanes x 4
+// token pairs x 4 bytes), so they are free of bank conflicts.
 // ---------------------------------------------------------------------
 
 constexpr int kTok = 8;
+constexpr int kTokThreads = 512;
 
 __device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, int src_bytes) {
     const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
@@ -20,53 +36,28 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// re-read of a shared-memory slot in the output pass: volatile, so the
-// compiler cannot keep the statistics pass's values alive instead
-__device__ __forceinline__ void lds16_again(uint32_t *r, const uint4 *p) {
-    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
-}
-
-template <DT T>
-__device__ __forceinline__ void push_tokens(f2_t *m, f2_t *q, const uint4 &v, float r) {
-    push2(m[0], q[0], f2(lo_f32<T>(v.x), hi_f32<T>(v.x)), r);
-    push2(m[1], q[1], f2(lo_f32<T>(v.y), hi_f32<T>(v.y)), r);
-    push2(m[2], q[2], f2(lo_f32<T>(v.z), hi_f32<T>(v.z)), r);
-    push2(m[3], q[3], f2(lo_f32<T>(v.w), hi_f32<T>(v.w)), r);
-}
-
-// chan(lower, upper) on 4 token pairs; `own` is this thread's state
-__device__ __forceinline__ void chan_tokens(f2_t *m, f2_t *q, float &cnt, const f2_t *pm,
-                                            const f2_t *pq, float pcnt, bool lower) {
-    float n;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (lower) {
-            chan2(m[k], q[k], cnt, pm[k], pq[k], pcnt, n);
-        } else {
-            f2_t mm = pm[k], qq = pq[k];
-            chan2(mm, qq, pcnt, m[k], q[k], cnt, n);
-            m[k] = mm;
-            q[k] = qq;
-        }
-    }
-    cnt = n;
+__device__ __forceinline__ uint32_t lds32(const void *p) {
+    uint32_t r;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)));
+    return r;
 }
 
 template <DT T, int NI>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kTokThreads, 2)
 ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB, int64_t sxD,
                  const uint16_t *scale, int64_t s_scale_b, const uint16_t *shift,
                  int64_t s_shift_b, float eps, int64_t tiles_per_b, int64_t ntiles) {
-    extern __shared__ __align__(16) uint4 tile[];  // [NI * 4][128], private per thread
-    __shared__ float xch[4][2 * kTok + 1];
+    extern __shared__ __align__(16) uint4 tile[];   // [NI * 4][128] rows of 8 tokens
+    __shared__ __align__(16) float st_mean[kTok][128];
+    __shared__ __align__(16) float st_m2[kTok][128];
     __shared__ float fin[2][kTok];
-    const int l = threadIdx.x;
-    const int wid = l >> 5;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int p = tid & 3;
+    const int l = warp * 8 + ((tid >> 2) & 7);
     const int nvec = D >> 2;
     const float Df = (float)D;
-    const float cnt0 = (l < nvec) ? 4.0f * (float)((nvec - 1 - l) / 128 + 1) : 0.0f;
+    const unsigned char *tb = reinterpret_cast<const unsigned char *>(tile);
     pdl_wait();
 
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -75,77 +66,59 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
         const int ntok = (int)imin64(kTok, N - n0);
         const uint16_t *xb = x + b * sxB + n0;
 
-        // every thread copies exactly the d-rows of its own logical lane
+        // 1. this thread's share of the lane's rows: element e = p of each chunk
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
             if (128 * i + l < nvec) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int64_t d = 4 * (128 * i + l) + e;
-                    cp_async16_zfill(&tile[(i * 4 + e) * 128 + l], xb + d * sxD, 2 * ntok);
-                }
+                const int64_t d = 4 * (128 * i + l) + p;
+                cp_async16_zfill(&tile[(i * 4 + p) * 128 + l], xb + d * sxD, 2 * ntok);
             }
             cp_async_commit();
         }
 
-        f2_t m[4], q[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) m[k] = q[k] = f2(0.f, 0.f);
+        // 2. pass 1: Welford of lane l, tokens 2p and 2p+1
+        f2_t m = f2(0.f, 0.f), q = m;
         static_for<0, NI>([&](auto I) {
             constexpr int i = decltype(I)::value;
             cp_async_wait<NI - 1 - i>();
+            __syncwarp();
             if (128 * i + l < nvec) {
                 static_for<0, 4>([&](auto E) {
                     constexpr int e = decltype(E)::value;
-                    const uint4 v = tile[(i * 4 + e) * 128 + l];
-                    push_tokens<T>(m, q, v, Rcp<4 * i + e + 1>::value);
+                    const uint32_t v = *reinterpret_cast<const uint32_t *>(
+                        tb + 16 * ((i * 4 + e) * 128 + l) + 4 * p);
+                    push2(m, q, f2(lo_f32<T>(v), hi_f32<T>(v)), Rcp<4 * i + e + 1>::value);
                 });
             }
         });
+        f2_split(m, st_mean[2 * p][l], st_mean[2 * p + 1][l]);
+        f2_split(q, st_m2[2 * p][l], st_m2[2 * p + 1][l]);
+        __syncthreads();
 
-        // fold inside the warp: offsets 16, 8, 4, 2, 1
-        float cnt = cnt0;
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            f2_t pm[4], pq[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                pm[k] = __shfl_xor_sync(0xffffffffu, m[k], off);
-                pq[k] = __shfl_xor_sync(0xffffffffu, q[k], off);
+        // 3. warp w < 8 folds token w over the 128 lanes
+        if (warp < kTok) {
+            const int u = tid & 31;
+            const float4 mv = *reinterpret_cast<const float4 *>(&st_mean[warp][4 * u]);
+            const float4 qv = *reinterpret_cast<const float4 *>(&st_m2[warp][4 * u]);
+            Stat s4[4] = {{mv.x, qv.x, lane_count128(4 * u, nvec)},
+                          {mv.y, qv.y, lane_count128(4 * u + 1, nvec)},
+                          {mv.z, qv.z, lane_count128(4 * u + 2, nvec)},
+                          {mv.w, qv.w, lane_count128(4 * u + 3, nvec)}};
+            const Stat f = fold128_k4(s4);
+            if (u == 0) {
+                fin[0][warp] = f.mean;
+                fin[1][warp] = finish_rstd(f.m2, Df, eps);
             }
-            const float pc = __shfl_xor_sync(0xffffffffu, cnt, off);
-            chan_tokens(m, q, cnt, pm, pq, pc, (l & off) == 0);
-        }
-        // offsets 64 then 32 across the four warps
-        if ((l & 31) == 0) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                f2_split(m[k], xch[wid][2 * k], xch[wid][2 * k + 1]);
-                f2_split(q[k], xch[wid][kTok + 2 * k], xch[wid][kTok + 2 * k + 1]);
-            }
-            xch[wid][2 * kTok] = cnt;
         }
         __syncthreads();
-        if (l < kTok) {
-            Stat g[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) g[w] = Stat{xch[w][l], xch[w][kTok + l], xch[w][2 * kTok]};
-            const Stat f = chan(chan(g[0], g[2]), chan(g[1], g[3]));
-            fin[0][l] = f.mean;
-            fin[1][l] = finish_rstd(f.m2, Df, eps);
-        }
-        __syncthreads();
-        f2_t mean2[4], rstd2[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            mean2[k] = f2(fin[0][2 * k], fin[0][2 * k + 1]);
-            rstd2[k] = f2(fin[1][2 * k], fin[1][2 * k + 1]);
-        }
 
-        // pass 2: this lane's d-rows, 8 tokens each, out rows contiguous in d
+        // 4. pass 2: tokens 2p, 2p+1 of lane l
+        const f2_t mean2 = f2(fin[0][2 * p], fin[0][2 * p + 1]);
+        const f2_t rstd2 = f2(fin[1][2 * p], fin[1][2 * p + 1]);
         const uint16_t *scr = scale + b * s_scale_b;
         const uint16_t *shr = shift + b * s_shift_b;
         uint16_t *ob = out + (b * N + n0) * (int64_t)D;
+        const bool st0 = 2 * p < ntok, st1 = 2 * p + 1 < ntok;
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
             const int j = 128 * i + l;
@@ -155,31 +128,28 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
                 ld_keep8(sh, shr + 4 * j);
                 const uint32_t op01 = add16x2<T>(sc[0], one16x2<T>());
                 const uint32_t op23 = add16x2<T>(sc[1], one16x2<T>());
-                float y[4][kTok];
+                float y0[4], y1[4];  // token 2p / 2p+1, element e of the chunk
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    uint32_t w[4];
-                    lds16_again(w, &tile[(i * 4 + e) * 128 + l]);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float xl, xh;
-                        unpack_again<T>(w[k], xl, xh);
-                        const f2_t u = f2_mul(f2_sub(f2(xl, xh), mean2[k]), rstd2[k]);
-                        f2_split(u, y[e][2 * k], y[e][2 * k + 1]);
-                    }
+                    const uint32_t v = lds32(tb + 16 * ((i * 4 + e) * 128 + l) + 4 * p);
+                    float xl, xh;
+                    unpack_again<T>(v, xl, xh);
+                    f2_split(f2_mul(f2_sub(f2(xl, xh), mean2), rstd2), y0[e], y1[e]);
                 }
-#pragma unroll
-                for (int tk = 0; tk < kTok; ++tk) {
-                    if (tk < ntok) {
-                        uint32_t o[2];
-                        o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y[0][tk], y[1][tk]), op01), sh[0]);
-                        o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y[2][tk], y[3][tk]), op23), sh[1]);
-                        st8(ob + tk * (int64_t)D + 4 * j, o);
-                    }
+                uint32_t o[2];
+                if (st0) {
+                    o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0[0], y0[1]), op01), sh[0]);
+                    o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0[2], y0[3]), op23), sh[1]);
+                    st8(ob + (2 * p) * (int64_t)D + 4 * j, o);
+                }
+                if (st1) {
+                    o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y1[0], y1[1]), op01), sh[0]);
+                    o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y1[2], y1[3]), op23), sh[1]);
+                    st8(ob + (2 * p + 1) * (int64_t)D + 4 * j, o);
                 }
             }
         }
-        __syncthreads();  // xch / fin are reused by the next tile
+        __syncthreads();  // the tile, st_* and fin are reused by the next tile
     }
     pdl_trigger();
 }
@@ -238,15 +208,18 @@ ln_generic_kernel(uint16_t *out, const uint16_t *x, int64_t B, int64_t N, int64_
 template <DT T, int NI>
 static cudaError_t run_tokens(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     auto k = ln_tokens_kernel<T, NI>;
-    const size_t smem = (size_t)NI * 4 * 128 * sizeof(uint4);
-    if (smem > 48 * 1024) {
+    const size_t smem = (size_t)NI * 4 * 128 * sizeof(uint4);  // + 8.1 KB static
+    static bool attr_done[64] = {};  // per device, for this (dtype, NI)
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    if (!attr_done[dev.device]) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
+        attr_done[dev.device] = true;
     }
     const int64_t tiles_per_b = (a.N + kTok - 1) / kTok;
     const int64_t ntiles = a.B * tiles_per_b;
-    const int64_t grid = imin64(ntiles, (int64_t)dev.sms * blocks_per_sm(k, 128, smem));
-    return launch_k(k, dim3((unsigned)grid), dim3(128), smem, s, pdl, (uint16_t *)a.out,
+    const int64_t grid = imin64(ntiles, (int64_t)dev.sms * blocks_per_sm(k, kTokThreads, smem));
+    return launch_k(k, dim3((unsigned)grid), dim3(kTokThreads), smem, s, pdl, (uint16_t *)a.out,
                     (const uint16_t *)a.x, a.N, (int)a.D, a.sxB, a.sxD, (const uint16_t *)a.scale,
                     a.s_scale_b, (const uint16_t *)a.shift, a.s_shift_b, a.eps, tiles_per_b, ntiles);
 }

@@ -184,20 +184,21 @@ def make_workloads(dev, which):
         w = synth.ln_tiny()
         x, sc, sh = (torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift"))
         o = torch.empty_like(x)
-        out["tiny"] = (lambda: ad.ln_modulate(x, sc, sh, 1e-6, out=o), ln_bytes(1, 64, 512), w.name)
+        out["tiny"] = (lambda x=x, sc=sc, sh=sh, o=o: ad.ln_modulate(x, sc, sh, 1e-6, out=o),
+                       ln_bytes(1, 64, 512), w.name)
     if "glm_ln" in which or "glm_gate" in which:
         w = synth.ln_glm()
         x, sc, sh = (torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift"))
         o = torch.empty_like(x)
         if "glm_ln" in which:
-            out["glm_ln"] = (lambda: ad.ln_modulate(x, sc, sh, 1e-5, out=o), ln_bytes(1, 4096, 4096),
-                             w.name)
+            out["glm_ln"] = (lambda x=x, sc=sc, sh=sh, o=o: ad.ln_modulate(x, sc, sh, 1e-5, out=o),
+                             ln_bytes(1, 4096, 4096), w.name)
         if "glm_gate" in which:
             wg = synth.gate_add_glm()
             y = torch_bits(wg.tensors["y"].draw(), "bf16", dev)
             g = torch_bits(wg.tensors["gate"].draw(), "bf16", dev)
             o2 = torch.empty_like(x)
-            out["glm_gate"] = (lambda: ad.residual_gate_add(x, g, y, out=o2),
+            out["glm_gate"] = (lambda x=x, g=g, y=y, o2=o2: ad.residual_gate_add(x, g, y, out=o2),
                                3 * 4096 * 4096 * 2 + 4096 * 2, wg.name)
     if "qk" in which:
         w = synth.qk_glm()
@@ -205,7 +206,8 @@ def make_workloads(dev, which):
         ws = [torch_bits(w.tensors[n].draw(), "bf16", dev) for n in ("wq", "bq", "wk", "bk")]
         qo, ko = torch.empty_like(q), torch.empty_like(k)
         rows = 4360 * 32
-        out["qk"] = (lambda: ad.qk_head_layernorm(q, k, *ws, 1e-6, q_out=qo, k_out=ko),
+        out["qk"] = (lambda q=q, k=k, ws=ws, qo=qo, ko=ko: ad.qk_head_layernorm(q, k, *ws, 1e-6, q_out=qo,
+                                                                                  k_out=ko),
                      2 * 2 * rows * 128 * 2 + 4 * 128 * 2, w.name)
     for dt in ("bf16", "fp16"):
         key = f"gelu_{dt}"
@@ -231,7 +233,7 @@ class Flusher:
     def __call__(self):
         import torch
         self.w.fill_(1.0)
-        torch.sum(self.r, out=self.sink)
+        torch.sum(self.r, dim=0, out=self.sink)
 
 
 def time_calls(fn, steps, warmup, flush, on_begin=None, on_end=None):
@@ -374,7 +376,7 @@ def run_ours(args):
     ad.init(local)
     flush = Flusher(dev)
 
-    main = make_workloads(dev, ["sana"])["sana"]
+    main = make_workloads(dev, [args.only])[args.only]
     fn, nbytes, wname = main
     sampler = ClockSampler(local)
     sampler.start()
@@ -462,6 +464,11 @@ def main():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--quick", action="store_true", help="headline only (for profiler runs)")
+    p.add_argument("--only", default="sana",
+                   choices=["sana", "sana_nmod2", "tiny", "glm_ln", "glm_gate", "qk", "gelu_bf16",
+                            "gelu_fp16"],
+                   help="workload timed as the headline (profiling runs); the JSON line's metric "
+                        "and roofline describe the Sana LN+modulate only when this is 'sana'")
     args = p.parse_args()
     if args.quick:
         args.no_per_config = args.no_cpu = args.no_e2e = True

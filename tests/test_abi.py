@@ -9,8 +9,7 @@ import pytest
 @pytest.fixture(scope="module")
 def ad():
     import __graft_entry__
-    from adaln_modulate_gb300 import _build
-    _build.build()
+    __graft_entry__.build()
     import adaln_modulate_gb300
     return adaln_modulate_gb300
 
