@@ -54,6 +54,137 @@ __device__ __forceinline__ float lane_count128(int l, int nvec) {
     return l < nvec ? 4.0f * (float)((nvec - 1 - l) / 128 + 1) : 0.0f;
 }
 
+// ---------------------------------------------------------------------
+// The fold with the "stride-8" lane mapping: thread u of a warp holds the
+// logical lanes l0 + 8s, s = 0..3, with l0 = (u & 7) + 32 (u >> 3).  The
+// butterfly offsets then map to
+//   16, 8      inside the thread (s bit 1, then s bit 0),
+//   4, 2, 1    thread xor 4, 2, 1,
+//   64, 32     thread xor 16, 8,
+// so after the two in-thread stages only one state crosses threads.
+//
+// Chan's coefficient of a stage, coef = n_upper / (n_lower + n_upper), and
+// the lower side's count n_lower depend only on D (the lanes' counts), not
+// on the data; FoldPlan holds them for one thread.  When every lane holds
+// the same number of chunks (D % 512 == 0) they are compile-time constants:
+// coef = 1/2 exactly and n_lower doubles from 4*NI at every stage.
+// ---------------------------------------------------------------------
+
+struct FoldPlan {
+    float c16[2], n16[2];  // in-thread offset 16: pairs (s0, s2), (s1, s3)
+    float c8, n8;          // in-thread offset 8
+    float c[5], n[5];      // offsets 4, 2, 1, 64, 32
+};
+static_assert(sizeof(FoldPlan) == 16 * sizeof(float), "FoldPlan is 16 floats");
+
+__host__ __device__ constexpr FoldPlan fold_plan_uniform(int NI) {
+    FoldPlan p{};
+    const float n1 = 4.0f * (float)NI;
+    p.c16[0] = p.c16[1] = 0.5f;
+    p.n16[0] = p.n16[1] = n1;
+    p.c8 = 0.5f;
+    p.n8 = 2.0f * n1;
+    float n = 4.0f * n1;
+    for (int k = 0; k < 5; ++k) {
+        p.c[k] = 0.5f;
+        p.n[k] = n;
+        n *= 2.0f;
+    }
+    return p;
+}
+
+// merged count of the lanes (rep & ~M) | k, k over the subsets of the
+// offset bits M already folded
+__device__ __forceinline__ float merged_count(int rep, int M, int nvec) {
+    float n = 0.0f;
+    const int base = rep & ~M;
+    for (int k = M;; k = (k - 1) & M) {  // every subset of M, exactly once
+        n += lane_count128(base | k, nvec);
+        if (k == 0) break;
+    }
+    return n;
+}
+
+__device__ __forceinline__ void plan_stage(int lower_rep, int upper_rep, int M, int nvec, float &c,
+                                           float &n_lower) {
+    const float a = merged_count(lower_rep, M, nvec), b = merged_count(upper_rep, M, nvec);
+    const float n = __fadd_rn(a, b);
+    c = (n == 0.0f) ? 0.0f : __fdiv_rn(b, n);
+    n_lower = a;
+}
+
+// plan for thread u of a warp (any D)
+__device__ __forceinline__ FoldPlan fold_plan_runtime(int u, int nvec) {
+    FoldPlan p;
+    const int l0 = (u & 7) + 32 * (u >> 3);
+    plan_stage(l0, l0 + 16, 0, nvec, p.c16[0], p.n16[0]);
+    plan_stage(l0 + 8, l0 + 24, 0, nvec, p.c16[1], p.n16[1]);
+    plan_stage(l0, l0 + 8, 16, nvec, p.c8, p.n8);
+    const int offs[5] = {4, 2, 1, 64, 32};
+    int M = 16 | 8;
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int o = offs[k];
+        plan_stage(l0 & ~o, l0 | o, M, nvec, p.c[k], p.n[k]);
+        M |= o;
+    }
+    return p;
+}
+
+// Chan's combine with a precomputed coefficient: (ma, qa) is the lower
+// lane's state and becomes the merged state.
+__device__ __forceinline__ void chan_p(float &ma, float &qa, float mb, float qb, float coef, float na) {
+    const float delta = __fsub_rn(mb, ma);
+    const float m = __fmaf_rn(delta, coef, ma);
+    qa = __fmaf_rn(__fmul_rn(__fmul_rn(delta, delta), na), coef, __fadd_rn(qa, qb));
+    ma = m;
+}
+
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+    f2_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// the same on two lane pairs at once: lower (ma, qa), upper (mb, qb)
+__device__ __forceinline__ void chan_p2(f2_t &ma, f2_t &qa, f2_t mb, f2_t qb, f2_t coef, f2_t na) {
+    const f2_t delta = f2_sub(mb, ma);
+    const f2_t m = f2_fma(delta, coef, ma);
+    qa = f2_fma(f2_mul(f2_mul(delta, delta), na), coef, f2_add(qa, qb));
+    ma = m;
+}
+
+// butterfly stage across threads: both partners end with
+// combine(lower, upper); `mask` is the thread-index bit of the stage
+__device__ __forceinline__ void shfl_stage_p(float &m, float &q, int mask, float coef, float na) {
+    const float pm = __shfl_xor_sync(0xffffffffu, m, mask);
+    const float pq = __shfl_xor_sync(0xffffffffu, q, mask);
+    const bool lower = (threadIdx.x & mask) == 0;
+    const float lo = lower ? m : pm, up = lower ? pm : m;
+    const float delta = __fsub_rn(up, lo);
+    m = __fmaf_rn(delta, coef, lo);
+    q = __fmaf_rn(__fmul_rn(__fmul_rn(delta, delta), na), coef, __fadd_rn(q, pq));
+}
+
+// Fold of the 4 lane states of every thread of a warp (stride-8 mapping):
+// m01 / q01 hold lanes s0, s1 and m23 / q23 lanes s2, s3.  Returns the
+// 128-lane (mean, m2) in every thread.
+__device__ __forceinline__ void fold128_s8(f2_t m01, f2_t q01, f2_t m23, f2_t q23, const FoldPlan &p,
+                                           float &mean, float &m2) {
+    chan_p2(m01, q01, m23, q23, f2(p.c16[0], p.c16[1]), f2(p.n16[0], p.n16[1]));  // offset 16
+    float m0, m1, q0, q1;
+    f2_split(m01, m0, m1);
+    f2_split(q01, q0, q1);
+    chan_p(m0, q0, m1, q1, p.c8, p.n8);                                          // offset 8
+    shfl_stage_p(m0, q0, 4, p.c[0], p.n[0]);
+    shfl_stage_p(m0, q0, 2, p.c[1], p.n[1]);
+    shfl_stage_p(m0, q0, 1, p.c[2], p.n[2]);
+    shfl_stage_p(m0, q0, 16, p.c[3], p.n[3]);
+    shfl_stage_p(m0, q0, 8, p.c[4], p.n[4]);
+    mean = m0;
+    m2 = q0;
+}
+
 __device__ __forceinline__ float finish_rstd(float m2, float Df, float eps) {
     return rsqrt_cr(__fadd_rn(__fdiv_rn(m2, Df), eps));
 }
@@ -62,7 +193,7 @@ __device__ __forceinline__ float finish_rstd(float m2, float Df, float eps) {
 static inline bool ln_aligned(const void *p, int a) { return ((uintptr_t)p % (uintptr_t)a) == 0; }
 static inline bool ln_mult(int64_t v, int64_t a) { return v % a == 0; }
 
-int ln_rows_vec_bytes(const LnArgs &a);
+bool ln_rows_ok(const LnArgs &a);
 constexpr int kRowsMaxNI = 8;     // contiguous rows in registers: D <= 4096
 constexpr int kTokensMaxNI = 12;  // tokens tile in shared memory: D <= 6144
 cudaError_t ln_rows_bf16(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev);

@@ -11,8 +11,8 @@
 // The rounding DAG is fixed by 128 LOGICAL lanes; the kernels below map
 // them onto threads differently but compute the same bits:
 //   ln_rows_kernel    contiguous rows, one warp per row, 4 logical lanes per
-//                     thread (16 consecutive elements = one 32-byte access
-//                     per 512-element step), row held in registers;
+//                     thread (lanes l0 + 8s, one 8-byte access each per
+//                     512-element step), row held in registers;
 //   ln_tokens_kernel  the (B, N, D) view of a contiguous (B, D, N) tensor
 //                     (tokens contiguous): a CTA takes 8 consecutive tokens,
 //                     one thread per logical lane for all 8, 16-byte
@@ -24,24 +24,19 @@
 
 namespace adaln {
 
-// Widest access (32/16/8 bytes) valid for every row start of x, out, scale
-// and shift of a contiguous-rows call, 0 if none.  Inside a row every
-// access starts at a multiple of 16 elements, so only row starts matter.
-// Strides of size-1 dimensions are never used and are ignored.
-int ln_rows_vec_bytes(const LnArgs &a) {
-    for (int vb : {32, 16, 8}) {
-        const int64_t ve = vb / 2;
-        const bool ok = ln_aligned(a.x, vb) && ln_aligned(a.out, vb) && ln_aligned(a.scale, vb) &&
-                        ln_aligned(a.shift, vb) && ln_mult(a.D, ve) && (a.N == 1 || ln_mult(a.sxN, ve)) &&
-                        (a.B == 1 || (ln_mult(a.sxB, ve) && ln_mult(a.s_scale_b, ve) && ln_mult(a.s_shift_b, ve)));
-        if (ok) return vb;
-    }
-    return 0;
+// The contiguous-rows kernel moves every logical lane's vec4 chunk with one
+// 8-byte access, so every row start of x, out, scale and shift must be
+// 8-byte aligned.  Strides of size-1 dimensions are never used and are
+// ignored.
+bool ln_rows_ok(const LnArgs &a) {
+    return ln_aligned(a.x, 8) && ln_aligned(a.out, 8) && ln_aligned(a.scale, 8) && ln_aligned(a.shift, 8) &&
+           (a.N == 1 || ln_mult(a.sxN, 4)) &&
+           (a.B == 1 || (ln_mult(a.sxB, 4) && ln_mult(a.s_scale_b, 4) && ln_mult(a.s_shift_b, 4)));
 }
 
 int ln_modulate_path(const LnArgs &a) {
     const int64_t ni = (a.D + 511) / 512;
-    if (a.sxD == 1 && ni <= kRowsMaxNI && ln_rows_vec_bytes(a) >= 8) return LN_PATH_ROWS;
+    if (a.sxD == 1 && ni <= kRowsMaxNI && ln_rows_ok(a)) return LN_PATH_ROWS;
     // tokens contiguous: each d-row of 8 tokens is one 16-byte copy
     if (a.sxN == 1 && a.sxD != 1 && a.N > 1 && ni <= kTokensMaxNI && ln_aligned(a.x, 16) &&
         ln_mult(a.sxD, 8) && (a.B == 1 || (ln_mult(a.sxB, 8) && ln_mult(a.s_scale_b, 4) && ln_mult(a.s_shift_b, 4))) &&

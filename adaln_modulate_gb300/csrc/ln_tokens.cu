@@ -15,8 +15,8 @@ namespace adaln {
 //   2. pass 1: serial Welford of lane l for tokens 2p, 2p+1 (one f32x2 op
 //      covers both tokens), state to shared memory;
 //   3. warps 0..7 fold token t = warp over the 128 lane states (4 lanes per
-//      thread, the same butterfly as the contiguous-rows kernel) and write
-//      mean / rstd of the token;
+//      thread in the stride-8 mapping of the contiguous-rows kernel, with
+//      the combine coefficients precomputed) and write mean / rstd;
 //   4. pass 2: thread (l, p) normalises its rows for its two tokens, applies
 //      the modulate and stores 4 consecutive d of each token (8 bytes).
 // Shared-memory reads of a warp cover 128 contiguous bytes (8 lanes x 4
@@ -25,6 +25,8 @@ namespace adaln {
 
 constexpr int kTok = 8;
 constexpr int kTokThreads = 512;
+constexpr int kStPitch = 128 + 24;
+__device__ __forceinline__ int st_idx(int l) { return l + 8 * (l >> 5); }
 
 __device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, int src_bytes) {
     const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
@@ -48,9 +50,12 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
                  const uint16_t *scale, int64_t s_scale_b, const uint16_t *shift,
                  int64_t s_shift_b, float eps, int64_t tiles_per_b, int64_t ntiles) {
     extern __shared__ __align__(16) uint4 tile[];   // [NI * 4][128] rows of 8 tokens
-    __shared__ __align__(16) float st_mean[kTok][128];
-    __shared__ __align__(16) float st_m2[kTok][128];
+    // lane states per token; lane l at l + 8 (l / 32) so that the fold
+    // warps' reads (lanes l0 + 8s) hit 32 distinct banks
+    __shared__ __align__(16) float st_mean[kTok][kStPitch];
+    __shared__ __align__(16) float st_m2[kTok][kStPitch];
     __shared__ float fin[2][kTok];
+    __shared__ float plan_s[16][32];  // fold coefficients of fold-warp thread u, field-major
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int p = tid & 3;
@@ -58,6 +63,12 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
     const int nvec = D >> 2;
     const float Df = (float)D;
     const unsigned char *tb = reinterpret_cast<const unsigned char *>(tile);
+    if (tid < 32) {
+        const FoldPlan pl = (D % 512 == 0) ? fold_plan_uniform(NI) : fold_plan_runtime(tid, nvec);
+        const float *f = reinterpret_cast<const float *>(&pl);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) plan_s[k][tid] = f[k];
+    }
     pdl_wait();
 
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -91,23 +102,37 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
                 });
             }
         });
-        f2_split(m, st_mean[2 * p][l], st_mean[2 * p + 1][l]);
-        f2_split(q, st_m2[2 * p][l], st_m2[2 * p + 1][l]);
+        f2_split(m, st_mean[2 * p][st_idx(l)], st_mean[2 * p + 1][st_idx(l)]);
+        f2_split(q, st_m2[2 * p][st_idx(l)], st_m2[2 * p + 1][st_idx(l)]);
+        // scale / shift of this lane's chunks do not depend on the statistics
+        const uint16_t *scr = scale + b * s_scale_b;
+        const uint16_t *shr = shift + b * s_shift_b;
+        uint32_t sc[NI][2], sh[NI][2];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int j = 128 * i + l;
+            if (j < nvec) {
+                ld_keep8(sc[i], scr + 4 * j);
+                ld_keep8(sh[i], shr + 4 * j);
+            }
+        }
         __syncthreads();
 
-        // 3. warp w < 8 folds token w over the 128 lanes
+        // 3. warp w < 8 folds token w over the 128 lanes (stride-8 mapping)
         if (warp < kTok) {
             const int u = tid & 31;
-            const float4 mv = *reinterpret_cast<const float4 *>(&st_mean[warp][4 * u]);
-            const float4 qv = *reinterpret_cast<const float4 *>(&st_m2[warp][4 * u]);
-            Stat s4[4] = {{mv.x, qv.x, lane_count128(4 * u, nvec)},
-                          {mv.y, qv.y, lane_count128(4 * u + 1, nvec)},
-                          {mv.z, qv.z, lane_count128(4 * u + 2, nvec)},
-                          {mv.w, qv.w, lane_count128(4 * u + 3, nvec)}};
-            const Stat f = fold128_k4(s4);
+            const int i0 = st_idx((u & 7) + 32 * (u >> 3));
+            const float *sm = st_mean[warp], *sq = st_m2[warp];
+            FoldPlan plan;
+            float *f = reinterpret_cast<float *>(&plan);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) f[k] = plan_s[k][u];
+            float mean, m2;
+            fold128_s8(f2(sm[i0], sm[i0 + 8]), f2(sq[i0], sq[i0 + 8]), f2(sm[i0 + 16], sm[i0 + 24]),
+                       f2(sq[i0 + 16], sq[i0 + 24]), plan, mean, m2);
             if (u == 0) {
-                fin[0][warp] = f.mean;
-                fin[1][warp] = finish_rstd(f.m2, Df, eps);
+                fin[0][warp] = mean;
+                fin[1][warp] = finish_rstd(m2, Df, eps);
             }
         }
         __syncthreads();
@@ -115,19 +140,14 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
         // 4. pass 2: tokens 2p, 2p+1 of lane l
         const f2_t mean2 = f2(fin[0][2 * p], fin[0][2 * p + 1]);
         const f2_t rstd2 = f2(fin[1][2 * p], fin[1][2 * p + 1]);
-        const uint16_t *scr = scale + b * s_scale_b;
-        const uint16_t *shr = shift + b * s_shift_b;
         uint16_t *ob = out + (b * N + n0) * (int64_t)D;
         const bool st0 = 2 * p < ntok, st1 = 2 * p + 1 < ntok;
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
             const int j = 128 * i + l;
             if (j < nvec) {
-                uint32_t sc[2], sh[2];
-                ld_keep8(sc, scr + 4 * j);
-                ld_keep8(sh, shr + 4 * j);
-                const uint32_t op01 = add16x2<T>(sc[0], one16x2<T>());
-                const uint32_t op23 = add16x2<T>(sc[1], one16x2<T>());
+                const uint32_t op01 = add16x2<T>(sc[i][0], one16x2<T>());
+                const uint32_t op23 = add16x2<T>(sc[i][1], one16x2<T>());
                 float y0[4], y1[4];  // token 2p / 2p+1, element e of the chunk
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -138,13 +158,13 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
                 }
                 uint32_t o[2];
                 if (st0) {
-                    o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0[0], y0[1]), op01), sh[0]);
-                    o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0[2], y0[3]), op23), sh[1]);
+                    o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0[0], y0[1]), op01), sh[i][0]);
+                    o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0[2], y0[3]), op23), sh[i][1]);
                     st8(ob + (2 * p) * (int64_t)D + 4 * j, o);
                 }
                 if (st1) {
-                    o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y1[0], y1[1]), op01), sh[0]);
-                    o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y1[2], y1[3]), op23), sh[1]);
+                    o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y1[0], y1[1]), op01), sh[i][0]);
+                    o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y1[2], y1[3]), op23), sh[i][1]);
                     st8(ob + (2 * p + 1) * (int64_t)D + 4 * j, o);
                 }
             }

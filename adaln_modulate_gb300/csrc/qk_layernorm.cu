@@ -8,172 +8,184 @@
 // var = m2 / Dh, rstd = rsqrt_rn(var + eps), out = round(fma(w, u, b)) with
 // u = rstd * (x - mean) in binary32.
 //
-// Mapping: 8 threads per row, 4 logical lanes (16 consecutive elements, one
-// 32-byte access) per thread; a warp normalises 4 rows at a time.  Logical
-// offsets 16, 8, 4 are thread xor 4, 2, 1 inside the 8-thread group and
-// offsets 2, 1 are inside the thread.
+// Mapping: one thread per (token, head) row.  The thread holds the row in
+// registers (Dh/4 vec4 chunks = logical lanes), runs the 32 Welford chains,
+// then the whole butterfly inside the thread on lane pairs (2k, 2k+1)
+// packed in f32x2 registers:
+//   offset 16: pairs k < 8 with k + 8,  offset 8: k < 4 with k + 4,
+//   offset 4: k < 2 with k + 2,  offset 2: pair 0 with pair 1,
+//   offset 1: the two halves of pair 0.
+// Chan's coefficients depend only on Dh (lanes past Dh/4 hold nothing); for
+// Dh = 128 they are 1/2 with the lower count 4, 8, 16, 32, 64.  The affine
+// (w, b) of q and of k are staged in shared memory as binary32.
 #include "common.cuh"
 #include "kernels.h"
+#include "ln_common.cuh"
 
 namespace adaln {
 
-constexpr int kQkThreads = 256;
+constexpr int kQkThreads = 128;
 
-__device__ __forceinline__ void qk_push2(f2_t &m, f2_t &q, f2_t v, float r) {
-    f2_t d = f2_sub(v, m);
-    f2_t m1 = f2_fma(d, f2(r, r), m);
-    q = f2_fma(d, f2_sub(v, m1), q);
-    m = m1;
+// Butterfly of the 32-lane DAG inside one thread.  Before the stage of
+// offset o, lane l (l < o) holds the lanes l + 2o t (t < 16/o) and its
+// partner l + o the lanes l + o + 2o t; lanes at or past nl hold nothing.
+__host__ __device__ constexpr float qk_count(int first, int o, int nl) {
+    float n = 0.0f;
+    for (int t = 0; t < 16 / o; ++t) n += (first + 2 * o * t < nl) ? 4.0f : 0.0f;
+    return n;
+}
+__host__ __device__ constexpr float qk_coef(int l, int o, int nl) {
+    const float a = qk_count(l, o, nl), b = qk_count(l + o, o, nl);
+    return (a + b == 0.0f) ? 0.0f : b / (a + b);
 }
 
-template <DT T> __device__ __forceinline__ void qk_load_affine(float *wf, float *bf, const uint16_t *w,
-                                                              const uint16_t *b, int col0, const bool *valid) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        uint32_t wr[2] = {0u, 0u}, br[2] = {0u, 0u};
-        if (valid[s]) {
-            ld_keep8(wr, w + col0 + 4 * s);
-            ld_keep8(br, b + col0 + 4 * s);
-        }
-        wf[4 * s + 0] = lo_f32<T>(wr[0]);
-        wf[4 * s + 1] = hi_f32<T>(wr[0]);
-        wf[4 * s + 2] = lo_f32<T>(wr[1]);
-        wf[4 * s + 3] = hi_f32<T>(wr[1]);
-        bf[4 * s + 0] = lo_f32<T>(br[0]);
-        bf[4 * s + 1] = hi_f32<T>(br[0]);
-        bf[4 * s + 2] = lo_f32<T>(br[1]);
-        bf[4 * s + 3] = hi_f32<T>(br[1]);
-    }
-}
-
-// FULL: Dh == 128 with 32-byte aligned rows (one v8 access per thread)
-template <DT T, bool FULL>
+// NL: logical lanes holding data (Dh / 4) as a compile-time constant (all
+// fold coefficients are then constants), or 0 for a run-time Dh.
+// VEC32: rows of 128 elements with 32-byte aligned starts.
+template <DT T, int NL, bool VEC32>
 __global__ void __launch_bounds__(kQkThreads)
 qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out,
              const uint16_t *k, int64_t rows_k, int Dh, const uint16_t *wq, const uint16_t *bq,
              const uint16_t *wk, const uint16_t *bk, float eps) {
-    pdl_wait();
-    const int sub = threadIdx.x & 7;
-    const int col0 = 16 * sub;
-    const int nvec = Dh >> 2;
+    __shared__ __align__(16) float aff[2][2][128];  // [q / k][w / b][column]
+    const int nl = NL ? NL : (Dh >> 2);
     const float Df = (float)Dh;
-    bool valid[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) valid[s] = FULL || (4 * sub + s < nvec);
-    float cnt[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) cnt[s] = valid[s] ? 4.0f : 0.0f;
+    pdl_wait();
+    for (int c = threadIdx.x; c < 128; c += kQkThreads) {
+        const bool in = c < Dh;
+        aff[0][0][c] = (in && rows_q) ? h_f32<T>(wq[c]) : 0.0f;
+        aff[0][1][c] = (in && rows_q) ? h_f32<T>(bq[c]) : 0.0f;
+        aff[1][0][c] = (in && rows_k) ? h_f32<T>(wk[c]) : 0.0f;
+        aff[1][1][c] = (in && rows_k) ? h_f32<T>(bk[c]) : 0.0f;
+    }
+    __syncthreads();
 
     const int64_t total = rows_q + rows_k;
-    // the row loop is uniform across the warp (its 4 groups take 4
-    // consecutive rows); groups past the end compute on zeros and store
-    // nothing, so every shuffle sees the full warp
-    const int64_t w0 = (((int64_t)blockIdx.x * kQkThreads + threadIdx.x) >> 5) * 4;
-    const int64_t wstride = ((int64_t)gridDim.x * kQkThreads >> 5) * 4;
-    const int grp = (threadIdx.x >> 3) & 3;
-
-    // affine of the tensor currently being processed (rows of q come first)
-    int cur = -1;
-    float wf[16], bf[16];
-
-    for (int64_t rb = w0; rb < total; rb += wstride) {
-        const int64_t r = rb + grp;
-        const bool active = r < total;
+    for (int64_t r = (int64_t)blockIdx.x * kQkThreads + threadIdx.x; r < total;
+         r += (int64_t)gridDim.x * kQkThreads) {
         const bool isq = r < rows_q;
-        const int which = isq ? 0 : 1;
-        if (active && which != cur) {
-            qk_load_affine<T>(wf, bf, isq ? wq : wk, isq ? bq : bk, col0, valid);
-            cur = which;
-        }
         const uint16_t *src = isq ? q + r * Dh : k + (r - rows_q) * Dh;
         uint16_t *dst = isq ? q_out + r * Dh : k_out + (r - rows_q) * Dh;
+        const float *w = aff[isq ? 0 : 1][0];
+        const float *bb = aff[isq ? 0 : 1][1];
 
-        uint32_t v[8];
-        if (!active) {
+        uint32_t v[32][2];  // lane l: elements 4l..4l+3
+        if constexpr (VEC32) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) v[kk] = 0u;
-        } else if (FULL) {
-            ld_stream32(v, src + col0);
+            for (int g = 0; g < 8; ++g) ld_stream32(&v[4 * g][0], src + 16 * g);
         } else {
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                if (valid[s]) {
-                    ld_stream8(&v[2 * s], src + col0 + 4 * s);
+            for (int l = 0; l < 32; ++l) {
+                if (l < nl) {
+                    ld_stream8(v[l], src + 4 * l);
                 } else {
-                    v[2 * s] = v[2 * s + 1] = 0u;
+                    v[l][0] = v[l][1] = 0u;
                 }
             }
         }
 
-        // Welford over the 4 elements of each logical lane (counts 1..4)
-        f2_t m01 = f2(0.f, 0.f), q01 = m01, m23 = m01, q23 = m01;
-        const float rc[4] = {Rcp<1>::value, Rcp<2>::value, Rcp<3>::value, Rcp<4>::value};
+        // Welford of every lane (counts 1..4) on lane pairs (2k, 2k+1);
+        // lanes at or past nl keep (0, 0)
+        f2_t m[16], qq[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int h = e >> 1;
-            float a0, a1, a2, a3;
-            if ((e & 1) == 0) {
-                a0 = lo_f32<T>(v[h]);
-                a1 = lo_f32<T>(v[2 + h]);
-                a2 = lo_f32<T>(v[4 + h]);
-                a3 = lo_f32<T>(v[6 + h]);
-            } else {
-                a0 = hi_f32<T>(v[h]);
-                a1 = hi_f32<T>(v[2 + h]);
-                a2 = hi_f32<T>(v[4 + h]);
-                a3 = hi_f32<T>(v[6 + h]);
+        for (int kp = 0; kp < 16; ++kp) {
+            m[kp] = qq[kp] = f2(0.f, 0.f);
+            if (2 * kp < nl) {
+                const uint32_t *a0 = v[2 * kp], *a1 = v[2 * kp + 1];
+                push2(m[kp], qq[kp], f2(lo_f32<T>(a0[0]), lo_f32<T>(a1[0])), Rcp<1>::value);
+                push2(m[kp], qq[kp], f2(hi_f32<T>(a0[0]), hi_f32<T>(a1[0])), Rcp<2>::value);
+                push2(m[kp], qq[kp], f2(lo_f32<T>(a0[1]), lo_f32<T>(a1[1])), Rcp<3>::value);
+                push2(m[kp], qq[kp], f2(hi_f32<T>(a0[1]), hi_f32<T>(a1[1])), Rcp<4>::value);
+                if (2 * kp + 1 >= nl) {  // the odd lane of the pair is past the end
+                    float x0, x1, y0, y1;
+                    f2_split(m[kp], x0, x1);
+                    f2_split(qq[kp], y0, y1);
+                    m[kp] = f2(x0, 0.f);
+                    qq[kp] = f2(y0, 0.f);
+                }
             }
-            qk_push2(m01, q01, f2(a0, a1), rc[e]);
-            qk_push2(m23, q23, f2(a2, a3), rc[e]);
         }
-        Stat st[4];
-        f2_split(m01, st[0].mean, st[1].mean);
-        f2_split(m23, st[2].mean, st[3].mean);
-        f2_split(q01, st[0].m2, st[1].m2);
-        f2_split(q23, st[2].m2, st[3].m2);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            if (!valid[s]) st[s].mean = st[s].m2 = 0.0f;  // a lane past Dh pushed nothing
-            st[s].cnt = cnt[s];
-        }
-#pragma unroll
-        for (int s = 0; s < 4; ++s) st[s] = shfl_stage(st[s], 4);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) st[s] = shfl_stage(st[s], 2);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) st[s] = shfl_stage(st[s], 1);
-        const Stat f = chan(chan(st[0], st[2]), chan(st[1], st[3]));
-        const float rstd = rsqrt_cr(__fadd_rn(__fdiv_rn(f.m2, Df), eps));
 
-        const f2_t mm = f2(f.mean, f.mean), rr = f2(rstd, rstd);
-        uint32_t o[8];
+        float mean, m2;
+        if constexpr (NL != 0) {
+            // offsets 16, 8, 4, 2 on lane pairs, offset 1 on the two halves
+#define QK_STAGE(O)                                                                  \
+    _Pragma("unroll") for (int kp = 0; kp < (O) / 2; ++kp) {                         \
+        chan_p2(m[kp], qq[kp], m[kp + (O) / 2], qq[kp + (O) / 2],                   \
+                f2(qk_coef(2 * kp, O, NL), qk_coef(2 * kp + 1, O, NL)),             \
+                f2(qk_count(2 * kp, O, NL), qk_count(2 * kp + 1, O, NL)));          \
+    }
+            QK_STAGE(16)
+            QK_STAGE(8)
+            QK_STAGE(4)
+            QK_STAGE(2)
+#undef QK_STAGE
+            float a0, a1, b0, b1;
+            f2_split(m[0], a0, a1);
+            f2_split(qq[0], b0, b1);
+            chan_p(a0, b0, a1, b1, qk_coef(0, 1, NL), qk_count(0, 1, NL));
+            mean = a0;
+            m2 = b0;
+        } else {
+            float lm[32], lq[32];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            f2_t u = f2(lo_f32<T>(v[kk]), hi_f32<T>(v[kk]));
-            u = f2_mul(f2_sub(u, mm), rr);
-            u = f2_fma(f2(wf[2 * kk], wf[2 * kk + 1]), u, f2(bf[2 * kk], bf[2 * kk + 1]));
-            float y0, y1;
-            f2_split(u, y0, y1);
-            o[kk] = pack_rn<T>(y0, y1);
+            for (int kp = 0; kp < 16; ++kp) {
+                f2_split(m[kp], lm[2 * kp], lm[2 * kp + 1]);
+                f2_split(qq[kp], lq[2 * kp], lq[2 * kp + 1]);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+                for (int l = 0; l < o; ++l) {
+                    const float a = qk_count(l, o, nl), b = qk_count(l + o, o, nl);
+                    const float n = __fadd_rn(a, b);
+                    const float c = (n == 0.0f) ? 0.0f : __fdiv_rn(b, n);
+                    chan_p(lm[l], lq[l], lm[l + o], lq[l + o], c, a);
+                }
+            }
+            mean = lm[0];
+            m2 = lq[0];
         }
-        if (!active) {
-            // nothing to store
-        } else if (FULL) {
-            st32(dst + col0, o);
+        const float rstd = rsqrt_cr(__fadd_rn(__fdiv_rn(m2, Df), eps));
+
+        // out = round(fma(w, rstd * (x - mean), b))
+        const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
+        uint32_t o[32][2];
+#pragma unroll
+        for (int l = 0; l < 32; ++l) {
+            if (l < nl) {
+                const float4 w4 = *reinterpret_cast<const float4 *>(w + 4 * l);
+                const float4 b4 = *reinterpret_cast<const float4 *>(bb + 4 * l);
+                float x0, x1, x2, x3, y0, y1, y2, y3;
+                unpack_again<T>(v[l][0], x0, x1);
+                unpack_again<T>(v[l][1], x2, x3);
+                f2_t u01 = f2_mul(f2_sub(f2(x0, x1), mm), rr);
+                f2_t u23 = f2_mul(f2_sub(f2(x2, x3), mm), rr);
+                u01 = f2_fma(f2(w4.x, w4.y), u01, f2(b4.x, b4.y));
+                u23 = f2_fma(f2(w4.z, w4.w), u23, f2(b4.z, b4.w));
+                f2_split(u01, y0, y1);
+                f2_split(u23, y2, y3);
+                o[l][0] = pack_rn<T>(y0, y1);
+                o[l][1] = pack_rn<T>(y2, y3);
+            }
+        }
+        if constexpr (VEC32) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) st32(dst + 16 * g, &o[4 * g][0]);
         } else {
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                if (valid[s]) st8(dst + col0 + 4 * s, &o[2 * s]);
+            for (int l = 0; l < 32; ++l)
+                if (l < nl) st8(dst + 4 * l, o[l]);
         }
     }
     pdl_trigger();
 }
 
-template <DT T, bool FULL>
+template <DT T, int NL, bool VEC32>
 static cudaError_t run_qk(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    auto kern = qk_ln_kernel<T, FULL>;
+    auto kern = qk_ln_kernel<T, NL, VEC32>;
     const int64_t total = a.rows_q + a.rows_k;
-    const int64_t ctas = (total * 8 + kQkThreads - 1) / kQkThreads;  // 32 rows per CTA pass
+    const int64_t ctas = (total + kQkThreads - 1) / kQkThreads;
     const int64_t grid = imin64(ctas, (int64_t)dev.sms * blocks_per_sm(kern, kQkThreads, 0));
     return launch_k(kern, dim3((unsigned)grid), dim3(kQkThreads), 0, s, pdl, (uint16_t *)a.q_out,
                     (const uint16_t *)a.q, a.rows_q, (uint16_t *)a.k_out, (const uint16_t *)a.k,
@@ -183,12 +195,17 @@ static cudaError_t run_qk(const QkArgs &a, bool pdl, cudaStream_t s, const Devic
 
 static bool al(const void *p, int a) { return p == nullptr || ((uintptr_t)p % (uintptr_t)a) == 0; }
 
+template <DT T>
+static cudaError_t qk_dispatch(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    const bool a32 = al(a.q, 32) && al(a.k, 32) && al(a.q_out, 32) && al(a.k_out, 32);
+    if (a.Dh == 128) return a32 ? run_qk<T, 32, true>(a, pdl, s, dev) : run_qk<T, 32, false>(a, pdl, s, dev);
+    if (a.Dh == 64) return run_qk<T, 16, false>(a, pdl, s, dev);
+    return run_qk<T, 0, false>(a, pdl, s, dev);
+}
+
 cudaError_t launch_qk_head_layernorm(const QkArgs &a, int dtype, bool pdl, cudaStream_t s,
                                      const DeviceInfo &dev) {
-    const bool full = a.Dh == 128 && al(a.q, 32) && al(a.k, 32) && al(a.q_out, 32) && al(a.k_out, 32);
-    if (dtype == 0)
-        return full ? run_qk<DT::BF16, true>(a, pdl, s, dev) : run_qk<DT::BF16, false>(a, pdl, s, dev);
-    return full ? run_qk<DT::FP16, true>(a, pdl, s, dev) : run_qk<DT::FP16, false>(a, pdl, s, dev);
+    return dtype == 0 ? qk_dispatch<DT::BF16>(a, pdl, s, dev) : qk_dispatch<DT::FP16>(a, pdl, s, dev);
 }
 
 }  // namespace adaln
