@@ -93,41 +93,44 @@ __host__ __device__ constexpr FoldPlan fold_plan_uniform(int NI) {
     return p;
 }
 
-// merged count of the lanes (rep & ~M) | k, k over the subsets of the
-// offset bits M already folded
-__device__ __forceinline__ float merged_count(int rep, int M, int nvec) {
-    float n = 0.0f;
-    const int base = rep & ~M;
-    for (int k = M;; k = (k - 1) & M) {  // every subset of M, exactly once
-        n += lane_count128(base | k, nvec);
-        if (k == 0) break;
+// Sum of the Welford counts of the lanes first, first + stride, ...
+// (n lanes).  Lane l (< 128) holds 4*(NI-1) + 4*[l < r] values, with
+// NI = ceil(nvec / 128) chunk steps and r = nvec - 128*(NI-1) lanes that
+// own a chunk in the last step.
+__device__ __forceinline__ float ap_count(int first, int stride, int n, int ni, int r) {
+    int below = 0;
+    if (first < r) {
+        below = (r - 1 - first) / stride + 1;
+        below = below < n ? below : n;
     }
-    return n;
+    return 4.0f * (float)((ni - 1) * n + below);
 }
 
-__device__ __forceinline__ void plan_stage(int lower_rep, int upper_rep, int M, int nvec, float &c,
-                                           float &n_lower) {
-    const float a = merged_count(lower_rep, M, nvec), b = merged_count(upper_rep, M, nvec);
+__device__ __forceinline__ void plan_coef(float a, float b, float &c, float &n_lower) {
     const float n = __fadd_rn(a, b);
     c = (n == 0.0f) ? 0.0f : __fdiv_rn(b, n);
     n_lower = a;
 }
 
-// plan for thread u of a warp (any D)
+// Plan for thread u of a warp, any D.  Along this butterfly every merged
+// lane set is an arithmetic progression (or two): before offset 16 the
+// single lanes; before 8 {l, l+16}; before 4 stride 8; before 2 stride 4;
+// before 1 stride 2; before 64 the 32 lanes of a group; before 32 two
+// groups.
 __device__ __forceinline__ FoldPlan fold_plan_runtime(int u, int nvec) {
     FoldPlan p;
+    const int ni = (nvec + 127) / 128;
+    const int r = nvec - 128 * (ni - 1);
     const int l0 = (u & 7) + 32 * (u >> 3);
-    plan_stage(l0, l0 + 16, 0, nvec, p.c16[0], p.n16[0]);
-    plan_stage(l0 + 8, l0 + 24, 0, nvec, p.c16[1], p.n16[1]);
-    plan_stage(l0, l0 + 8, 16, nvec, p.c8, p.n8);
-    const int offs[5] = {4, 2, 1, 64, 32};
-    int M = 16 | 8;
-#pragma unroll
-    for (int k = 0; k < 5; ++k) {
-        const int o = offs[k];
-        plan_stage(l0 & ~o, l0 | o, M, nvec, p.c[k], p.n[k]);
-        M |= o;
-    }
+    plan_coef(ap_count(l0, 1, 1, ni, r), ap_count(l0 + 16, 1, 1, ni, r), p.c16[0], p.n16[0]);
+    plan_coef(ap_count(l0 + 8, 1, 1, ni, r), ap_count(l0 + 24, 1, 1, ni, r), p.c16[1], p.n16[1]);
+    plan_coef(ap_count(l0, 16, 2, ni, r), ap_count(l0 + 8, 16, 2, ni, r), p.c8, p.n8);
+    plan_coef(ap_count(l0 & ~4, 8, 4, ni, r), ap_count(l0 | 4, 8, 4, ni, r), p.c[0], p.n[0]);
+    plan_coef(ap_count(l0 & ~6, 4, 8, ni, r), ap_count((l0 & ~6) | 2, 4, 8, ni, r), p.c[1], p.n[1]);
+    plan_coef(ap_count(l0 & ~7, 2, 16, ni, r), ap_count((l0 & ~7) | 1, 2, 16, ni, r), p.c[2], p.n[2]);
+    plan_coef(ap_count(l0 & 32, 1, 32, ni, r), ap_count((l0 & 32) + 64, 1, 32, ni, r), p.c[3], p.n[3]);
+    plan_coef(ap_count(0, 1, 32, ni, r) + ap_count(64, 1, 32, ni, r),
+              ap_count(32, 1, 32, ni, r) + ap_count(96, 1, 32, ni, r), p.c[4], p.n[4]);
     return p;
 }
 

@@ -7,24 +7,26 @@ namespace adaln {
 // ---------------------------------------------------------------------
 // tokens contiguous (transposed view): 8 tokens per CTA
 //
-// 512 threads; thread (l, p) is logical lane l = 8*warp + ((tid >> 2) & 7)
-// for the token pair p = tid & 3 (tokens 2p, 2p+1).  Data flow per tile:
-//   1. thread (l, p) copies the d-rows 4*(128*i + l) + p (8 tokens, 16 bytes
-//      each) into the tile with cp.async; the 4 threads of a lane sit in one
-//      warp, so a warp barrier makes a lane's 4 rows visible to all of them;
-//   2. pass 1: serial Welford of lane l for tokens 2p, 2p+1 (one f32x2 op
-//      covers both tokens), state to shared memory;
-//   3. warps 0..7 fold token t = warp over the 128 lane states (4 lanes per
-//      thread in the stride-8 mapping of the contiguous-rows kernel, with
-//      the combine coefficients precomputed) and write mean / rstd;
-//   4. pass 2: thread (l, p) normalises its rows for its two tokens, applies
+// 256 threads; thread (l, h) is logical lane l = 16*warp + ((tid >> 1) & 15)
+// for the tokens 4h .. 4h+3 (h = tid & 1), two f32x2 pairs.  Per tile:
+//   1. thread (l, h) copies the d-rows 4*(128*i + l) + 2h + {0, 1} (8
+//      tokens, 16 bytes each) into the tile with cp.async; both threads of
+//      a lane sit in one warp, so a warp barrier makes the lane's 4 rows
+//      visible to both;
+//   2. pass 1: serial Welford of lane l for its 4 tokens, states to shared
+//      memory;
+//   3. warps 0..3 fold the token pair (2w, 2w+1) over the 128 lane states
+//      (4 lanes per thread in the stride-8 mapping of the contiguous-rows
+//      kernel, one f32x2 op covering both tokens, coefficients from the
+//      fold plan) and write mean / rstd;
+//   4. pass 2: thread (l, h) normalises its rows for its 4 tokens, applies
 //      the modulate and stores 4 consecutive d of each token (8 bytes).
-// Shared-memory reads of a warp cover 128 contiguous bytes (8 lanes x 4
-// token pairs x 4 bytes), so they are free of bank conflicts.
+// Shared-memory reads of a warp cover 256 contiguous bytes (16 lanes x 2
+// halves x 8 bytes): two wavefronts, no bank conflict.
 // ---------------------------------------------------------------------
 
 constexpr int kTok = 8;
-constexpr int kTokThreads = 512;
+constexpr int kTokThreads = 256;
 constexpr int kStPitch = 128 + 24;
 __device__ __forceinline__ int st_idx(int l) { return l + 8 * (l >> 5); }
 
@@ -38,10 +40,38 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint32_t lds32(const void *p) {
-    uint32_t r;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)));
-    return r;
+// 8-byte shared load (volatile, so the output pass re-reads the tile rather
+// than keeping the statistics pass's values alive)
+__device__ __forceinline__ void lds64_again(uint32_t *r, uint32_t saddr) {
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(saddr));
+}
+
+// butterfly stage across threads on a token pair
+__device__ __forceinline__ void shfl_stage_p2(f2_t &m, f2_t &q, int mask, float coef, float na) {
+    const f2_t pm = __shfl_xor_sync(0xffffffffu, m, mask);
+    const f2_t pq = __shfl_xor_sync(0xffffffffu, q, mask);
+    const bool lower = (threadIdx.x & mask) == 0;
+    const f2_t lo = lower ? m : pm, up = lower ? pm : m;
+    const f2_t delta = f2_sub(up, lo);
+    const f2_t c = f2(coef, coef);
+    m = f2_fma(delta, c, lo);
+    q = f2_fma(f2_mul(f2_mul(delta, delta), f2(na, na)), c, f2_add(q, pq));
+}
+
+// the stride-8 fold of fold128_s8 on two tokens at once: sX holds lane
+// l0 + 8X of the thread for (token a, token b)
+__device__ __forceinline__ void fold128_s8_x2(f2_t m0, f2_t q0, f2_t m1, f2_t q1, f2_t m2, f2_t q2,
+                                              f2_t m3, f2_t q3, const FoldPlan &p, f2_t &mean, f2_t &m2o) {
+    chan_p2(m0, q0, m2, q2, f2(p.c16[0], p.c16[0]), f2(p.n16[0], p.n16[0]));  // offset 16, s0 + s2
+    chan_p2(m1, q1, m3, q3, f2(p.c16[1], p.c16[1]), f2(p.n16[1], p.n16[1]));  // offset 16, s1 + s3
+    chan_p2(m0, q0, m1, q1, f2(p.c8, p.c8), f2(p.n8, p.n8));                  // offset 8
+    shfl_stage_p2(m0, q0, 4, p.c[0], p.n[0]);
+    shfl_stage_p2(m0, q0, 2, p.c[1], p.n[1]);
+    shfl_stage_p2(m0, q0, 1, p.c[2], p.n[2]);
+    shfl_stage_p2(m0, q0, 16, p.c[3], p.n[3]);
+    shfl_stage_p2(m0, q0, 8, p.c[4], p.n[4]);
+    mean = m0;
+    m2o = q0;
 }
 
 template <DT T, int NI>
@@ -51,18 +81,20 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
                  int64_t s_shift_b, float eps, int64_t tiles_per_b, int64_t ntiles) {
     extern __shared__ __align__(16) uint4 tile[];   // [NI * 4][128] rows of 8 tokens
     // lane states per token; lane l at l + 8 (l / 32) so that the fold
-    // warps' reads (lanes l0 + 8s) hit 32 distinct banks
+    // warps' reads (lanes l0 + 8s) hit distinct banks
     __shared__ __align__(16) float st_mean[kTok][kStPitch];
     __shared__ __align__(16) float st_m2[kTok][kStPitch];
     __shared__ float fin[2][kTok];
-    __shared__ float plan_s[16][32];  // fold coefficients of fold-warp thread u, field-major
+    __shared__ float plan_s[16][32];  // fold plan of fold-warp thread u, field-major
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int p = tid & 3;
-    const int l = warp * 8 + ((tid >> 2) & 7);
+    const int h = tid & 1;
+    const int l = warp * 16 + ((tid >> 1) & 15);
     const int nvec = D >> 2;
     const float Df = (float)D;
-    const unsigned char *tb = reinterpret_cast<const unsigned char *>(tile);
+    const uint32_t tile_s = (uint32_t)__cvta_generic_to_shared(tile);
+    // this thread's 8 bytes of the lane-l slot of row group g: tile_s + 16*(g*128 + l) + 8h
+    const uint32_t my_s = tile_s + 16 * l + 8 * h;
     if (tid < 32) {
         const FoldPlan pl = (D % 512 == 0) ? fold_plan_uniform(NI) : fold_plan_runtime(tid, nvec);
         const float *f = reinterpret_cast<const float *>(&pl);
@@ -75,20 +107,24 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
         const int64_t b = t / tiles_per_b;
         const int64_t n0 = (t - b * tiles_per_b) * kTok;
         const int ntok = (int)imin64(kTok, N - n0);
-        const uint16_t *xb = x + b * sxB + n0;
+        // row d = 4j + e of lane l at step i, j = 128 i + l; this thread
+        // copies e = 2h and 2h + 1
+        const uint16_t *xl = x + b * sxB + n0 + (int64_t)(4 * l + 2 * h) * sxD;
+        const int64_t step_stride = 512 * sxD;
 
-        // 1. this thread's share of the lane's rows: element e = p of each chunk
+        // 1. copies
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
             if (128 * i + l < nvec) {
-                const int64_t d = 4 * (128 * i + l) + p;
-                cp_async16_zfill(&tile[(i * 4 + p) * 128 + l], xb + d * sxD, 2 * ntok);
+                const uint16_t *src = xl + i * step_stride;
+                cp_async16_zfill(&tile[(i * 4 + 2 * h) * 128 + l], src, 2 * ntok);
+                cp_async16_zfill(&tile[(i * 4 + 2 * h + 1) * 128 + l], src + sxD, 2 * ntok);
             }
             cp_async_commit();
         }
 
-        // 2. pass 1: Welford of lane l, tokens 2p and 2p+1
-        f2_t m = f2(0.f, 0.f), q = m;
+        // 2. pass 1: Welford of lane l, tokens 4h .. 4h+3
+        f2_t ma = f2(0.f, 0.f), qa = ma, mb = ma, qb = ma;
         static_for<0, NI>([&](auto I) {
             constexpr int i = decltype(I)::value;
             cp_async_wait<NI - 1 - i>();
@@ -96,76 +132,91 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
             if (128 * i + l < nvec) {
                 static_for<0, 4>([&](auto E) {
                     constexpr int e = decltype(E)::value;
-                    const uint32_t v = *reinterpret_cast<const uint32_t *>(
-                        tb + 16 * ((i * 4 + e) * 128 + l) + 4 * p);
-                    push2(m, q, f2(lo_f32<T>(v), hi_f32<T>(v)), Rcp<4 * i + e + 1>::value);
+                    uint32_t v[2];
+                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                                 : "=r"(v[0]), "=r"(v[1]) : "r"(my_s + 16 * 128 * (i * 4 + e)));
+                    constexpr float r = Rcp<4 * i + e + 1>::value;
+                    push2(ma, qa, f2(lo_f32<T>(v[0]), hi_f32<T>(v[0])), r);
+                    push2(mb, qb, f2(lo_f32<T>(v[1]), hi_f32<T>(v[1])), r);
                 });
             }
         });
-        f2_split(m, st_mean[2 * p][st_idx(l)], st_mean[2 * p + 1][st_idx(l)]);
-        f2_split(q, st_m2[2 * p][st_idx(l)], st_m2[2 * p + 1][st_idx(l)]);
+        {
+            const int si = st_idx(l);
+            f2_split(ma, st_mean[4 * h][si], st_mean[4 * h + 1][si]);
+            f2_split(mb, st_mean[4 * h + 2][si], st_mean[4 * h + 3][si]);
+            f2_split(qa, st_m2[4 * h][si], st_m2[4 * h + 1][si]);
+            f2_split(qb, st_m2[4 * h + 2][si], st_m2[4 * h + 3][si]);
+        }
         // scale / shift of this lane's chunks do not depend on the statistics
-        const uint16_t *scr = scale + b * s_scale_b;
-        const uint16_t *shr = shift + b * s_shift_b;
+        const uint16_t *scr = scale + b * s_scale_b + 4 * l;
+        const uint16_t *shr = shift + b * s_shift_b + 4 * l;
         uint32_t sc[NI][2], sh[NI][2];
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
-            const int j = 128 * i + l;
-            if (j < nvec) {
-                ld_keep8(sc[i], scr + 4 * j);
-                ld_keep8(sh[i], shr + 4 * j);
+            if (128 * i + l < nvec) {
+                ld_keep8(sc[i], scr + 512 * i);
+                ld_keep8(sh[i], shr + 512 * i);
             }
         }
         __syncthreads();
 
-        // 3. warp w < 8 folds token w over the 128 lanes (stride-8 mapping)
-        if (warp < kTok) {
+        // 3. warp w < 4 folds the token pair (2w, 2w + 1)
+        if (warp < kTok / 2) {
             const int u = tid & 31;
             const int i0 = st_idx((u & 7) + 32 * (u >> 3));
-            const float *sm = st_mean[warp], *sq = st_m2[warp];
+            const float *ma0 = st_mean[2 * warp], *ma1 = st_mean[2 * warp + 1];
+            const float *qa0 = st_m2[2 * warp], *qa1 = st_m2[2 * warp + 1];
             FoldPlan plan;
             float *f = reinterpret_cast<float *>(&plan);
 #pragma unroll
             for (int k = 0; k < 16; ++k) f[k] = plan_s[k][u];
-            float mean, m2;
-            fold128_s8(f2(sm[i0], sm[i0 + 8]), f2(sq[i0], sq[i0 + 8]), f2(sm[i0 + 16], sm[i0 + 24]),
-                       f2(sq[i0 + 16], sq[i0 + 24]), plan, mean, m2);
-            if (u == 0) {
-                fin[0][warp] = mean;
-                fin[1][warp] = finish_rstd(m2, Df, eps);
+            f2_t mean2, m22;
+            fold128_s8_x2(f2(ma0[i0], ma1[i0]), f2(qa0[i0], qa1[i0]), f2(ma0[i0 + 8], ma1[i0 + 8]),
+                          f2(qa0[i0 + 8], qa1[i0 + 8]), f2(ma0[i0 + 16], ma1[i0 + 16]),
+                          f2(qa0[i0 + 16], qa1[i0 + 16]), f2(ma0[i0 + 24], ma1[i0 + 24]),
+                          f2(qa0[i0 + 24], qa1[i0 + 24]), plan, mean2, m22);
+            if (u < 2) {
+                float mx, my, qx, qy;
+                f2_split(mean2, mx, my);
+                f2_split(m22, qx, qy);
+                fin[0][2 * warp + u] = u ? my : mx;
+                fin[1][2 * warp + u] = finish_rstd(u ? qy : qx, Df, eps);
             }
         }
         __syncthreads();
 
-        // 4. pass 2: tokens 2p, 2p+1 of lane l
-        const f2_t mean2 = f2(fin[0][2 * p], fin[0][2 * p + 1]);
-        const f2_t rstd2 = f2(fin[1][2 * p], fin[1][2 * p + 1]);
-        uint16_t *ob = out + (b * N + n0) * (int64_t)D;
-        const bool st0 = 2 * p < ntok, st1 = 2 * p + 1 < ntok;
+        // 4. pass 2: tokens 4h .. 4h+3 of lane l
+        const f2_t meanA = f2(fin[0][4 * h], fin[0][4 * h + 1]);
+        const f2_t meanB = f2(fin[0][4 * h + 2], fin[0][4 * h + 3]);
+        const f2_t rstdA = f2(fin[1][4 * h], fin[1][4 * h + 1]);
+        const f2_t rstdB = f2(fin[1][4 * h + 2], fin[1][4 * h + 3]);
+        uint16_t *ob = out + (b * N + n0 + 4 * h) * (int64_t)D + 4 * l;
+        const int nmine = ntok - 4 * h;  // tokens of this half that exist
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
-            const int j = 128 * i + l;
-            if (j < nvec) {
+            if (128 * i + l < nvec) {
                 const uint32_t op01 = add16x2<T>(sc[i][0], one16x2<T>());
                 const uint32_t op23 = add16x2<T>(sc[i][1], one16x2<T>());
-                float y0[4], y1[4];  // token 2p / 2p+1, element e of the chunk
+                float y[4][4];  // [element e of the chunk][token]
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const uint32_t v = lds32(tb + 16 * ((i * 4 + e) * 128 + l) + 4 * p);
-                    float xl, xh;
-                    unpack_again<T>(v, xl, xh);
-                    f2_split(f2_mul(f2_sub(f2(xl, xh), mean2), rstd2), y0[e], y1[e]);
+                    uint32_t v[2];
+                    lds64_again(v, my_s + 16 * 128 * (i * 4 + e));
+                    float x0, x1, x2, x3;
+                    unpack_again<T>(v[0], x0, x1);
+                    unpack_again<T>(v[1], x2, x3);
+                    f2_split(f2_mul(f2_sub(f2(x0, x1), meanA), rstdA), y[e][0], y[e][1]);
+                    f2_split(f2_mul(f2_sub(f2(x2, x3), meanB), rstdB), y[e][2], y[e][3]);
                 }
-                uint32_t o[2];
-                if (st0) {
-                    o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0[0], y0[1]), op01), sh[i][0]);
-                    o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0[2], y0[3]), op23), sh[i][1]);
-                    st8(ob + (2 * p) * (int64_t)D + 4 * j, o);
-                }
-                if (st1) {
-                    o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y1[0], y1[1]), op01), sh[i][0]);
-                    o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y1[2], y1[3]), op23), sh[i][1]);
-                    st8(ob + (2 * p + 1) * (int64_t)D + 4 * j, o);
+#pragma unroll
+                for (int tk = 0; tk < 4; ++tk) {
+                    if (tk < nmine) {
+                        uint32_t o[2];
+                        o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y[0][tk], y[1][tk]), op01), sh[i][0]);
+                        o[1] = add16x2<T>(mul16x2<T>(pack_rn<T>(y[2][tk], y[3][tk]), op23), sh[i][1]);
+                        st8(ob + tk * (int64_t)D + 512 * i, o);
+                    }
                 }
             }
         }
