@@ -55,6 +55,7 @@ _SIGS = {
     "adaln_can_residual_gate_add": ([_P, _P, _P, _I, _P, _I, _I, _I, _INT, _U], _INT),
     "adaln_bias_gelu_tanh": ([_P, _P, _P, _I, _I, _INT, _U, _P], _INT),
     "adaln_can_bias_gelu_tanh": ([_P, _P, _P, _I, _I, _INT, _U], _INT),
+    "adaln_bias_gelu_tanh_noalloc": ([_P, _P, _P, _I, _I, _INT, _U, _P], _INT),
 }
 
 

@@ -213,6 +213,41 @@ adaln_status adaln_can_bias_gelu_tanh(const void *out, const void *x, const void
                                       int64_t rows, int64_t width,
                                       int dtype, uint32_t flags);
 
+/* ------------------------------------------------------------------------
+ * adaln_bias_gelu_tanh_noalloc
+ *   The same operation, arguments, limits and results (bit for bit) as
+ *   adaln_bias_gelu_tanh, for callers that cannot let a library allocate
+ *   device memory.  The paper has no counterpart: this entry point exists
+ *   for the way some programs manage memory, not for the method.
+ *
+ *   Who needs it: a process whose memory pool or arena owns the whole device
+ *   (a server that plans every byte of HBM up front), code that must not
+ *   hit the implicit device synchronisation of cudaMalloc / cudaFree, or a
+ *   host program that forbids allocations after start-up.
+ *   adaln_bias_gelu_tanh allocates its lookup tables with cudaMalloc on
+ *   first use; this variant keeps them in a fixed array that is part of the
+ *   library's device image and calls no cudaMalloc, cudaFree or other
+ *   allocating routine.  The caller still allocates and owns x, bias, out.
+ *
+ *   Memory held: 256 KiB (one 65536-entry table per storage type) on every
+ *   GPU that loads the library, until the process exits.  Every call needs
+ *   one 128 KiB table inside it; a call whose table would not fit returns
+ *   ADALN_E_SHAPE (no bf16 / fp16 call does).
+ *
+ *   Set-up: the first call on a device for a storage type (made with that
+ *   device current) looks up the array's device address and fills that
+ *   storage type's table on `stream`, then waits for the stream to finish.
+ *   Make that first call before capturing `stream` into a CUDA graph.  The
+ *   table is written only by that first call; later calls only read the
+ *   shared array, and nothing in it has to start at zero.  A later call
+ *   that overlaps that first call's table build on another stream would
+ *   race with it, and a call after cudaDeviceReset would use an array whose
+ *   contents were lost; neither is detected.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_bias_gelu_tanh_noalloc(void *out, const void *x, const void *bias,
+                                          int64_t rows, int64_t width,
+                                          int dtype, uint32_t flags, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
