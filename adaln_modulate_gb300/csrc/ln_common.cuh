@@ -189,7 +189,7 @@ __device__ __forceinline__ void fold128_s8(f2_t m01, f2_t q01, f2_t m23, f2_t q2
 }
 
 __device__ __forceinline__ float finish_rstd(float m2, float Df, float eps) {
-    return rsqrt_cr(__fadd_rn(__fdiv_rn(m2, Df), eps));
+    return rsqrt_rn(__fadd_rn(__fdiv_rn(m2, Df), eps));
 }
 
 

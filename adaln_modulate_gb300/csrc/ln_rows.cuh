@@ -1,6 +1,6 @@
 // Contiguous-rows kernel of ln_modulate (one warp per row); instantiated per
-// storage type in ln_rows_bf16.cu / ln_rows_fp16.cu.  Every access is 8
-// bytes (one logical lane's vec4 chunk), so rows only need 8-byte aligned
+// storage type in ln_rows_bf16.cu / ln_rows_fp16.cu.  Every global access is
+// 8 bytes (one logical lane's vec4 chunk), so rows only need 8-byte aligned
 // starts.
 #pragma once
 #include "ln_common.cuh"
@@ -19,11 +19,21 @@ constexpr int kRowsThreads = 256;
 // access for a given s covers 4 runs of 64 contiguous bytes.  TAIL: D is
 // not a multiple of 512 (the last step masks lanes past D/4 and the fold
 // coefficients are computed per thread).
-template <DT T, int NI, bool TAIL>
-__global__ void __launch_bounds__(kRowsThreads)
-ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t N, int D, int64_t sxB,
-               int64_t sxN, const uint16_t *scale, int64_t s_scale_b, const uint16_t *shift,
-               int64_t s_shift_b, float eps) {
+//
+// OPSH: the modulate operands op = round(1 + scale) and shift of all B
+// samples are computed once per CTA into shared memory (B * D * 4 bytes, at
+// most kOpshMaxBytes), interleaved per column pair as (op, shift), so the
+// output pass reads one 16-byte shared word per lane chunk instead of two
+// global loads and an add per column pair.  Otherwise scale and shift are
+// read from global memory (L2) in the output pass.
+constexpr int kOpshMaxBytes = 32 * 1024;
+
+template <DT T, int NI, bool TAIL, bool OPSH>
+__global__ void __launch_bounds__(kRowsThreads, 2)
+ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_t N, int D,
+               int64_t sxB, int64_t sxN, const uint16_t *scale, int64_t s_scale_b,
+               const uint16_t *shift, int64_t s_shift_b, float eps) {
+    extern __shared__ __align__(16) uint32_t opsh[];  // OPSH: [b][column pair][op, shift]
     pdl_wait();
     const int u = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -48,13 +58,11 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t N, int D,
     const int64_t r0 = blockIdx.x * per + imin64(blockIdx.x, extra);
     const int64_t r1 = r0 + per + (blockIdx.x < extra ? 1 : 0);
 
-    for (int64_t row = r0 + warp; row < r1; row += kRowsThreads / 32) {
+    // xv[i][s] = the 4 elements of lane l0 + 8s at step i (2 registers)
+    uint32_t xv[NI][4][2];
+    auto load_row = [&](int64_t row) {
         const int64_t b = row / N;
-        const int64_t n = row - b * N;
-        const uint16_t *xr = x + b * sxB + n * sxN + c0;
-
-        // xv[i][s] = the 4 elements of lane l0 + 8s at step i (2 registers)
-        uint32_t xv[NI][4][2];
+        const uint16_t *xr = x + b * sxB + (row - b * N) * sxN + c0;
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
 #pragma unroll
@@ -66,6 +74,49 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t N, int D,
                 }
             }
         }
+    };
+    // the warp's row after `row`: one L2 prefetch request by lane 0, so that
+    // its DRAM reads overlap this row's work
+    auto prefetch_row = [&](int64_t row) {
+        if (u == 0 && row < r1) {
+            const int64_t b = row / N;
+            prefetch_l2_inner(x + b * sxB + (row - b * N) * sxN, (uint64_t)D * 2);
+        }
+    };
+
+    int64_t row = r0 + warp;
+    if (row < r1) load_row(row);
+    prefetch_row(row + kRowsThreads / 32);
+
+    if constexpr (OPSH) {
+        // all loads of a batch in flight before any is used
+        constexpr int kFill = 8;
+        const int half = D / 2, npairs = (int)B * half;  // npairs <= kOpshMaxBytes / 8
+        for (int base = 0; base < npairs; base += kFill * kRowsThreads) {
+            uint32_t s2[kFill], h2[kFill];
+#pragma unroll
+            for (int k = 0; k < kFill; ++k) {
+                const int e = base + k * kRowsThreads + threadIdx.x;
+                if (e < npairs) {
+                    const int bb = e / half, cp = e - bb * half;
+                    asm("ld.global.nc.b32 %0, [%1];" : "=r"(s2[k]) : "l"(scale + bb * s_scale_b + 2 * cp));
+                    asm("ld.global.nc.b32 %0, [%1];" : "=r"(h2[k]) : "l"(shift + bb * s_shift_b + 2 * cp));
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kFill; ++k) {
+                const int e = base + k * kRowsThreads + threadIdx.x;
+                if (e < npairs) {
+                    opsh[2 * e] = add16x2<T>(s2[k], one16x2<T>());
+                    opsh[2 * e + 1] = h2[k];
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    for (; row < r1; row += kRowsThreads / 32) {
+        const int64_t b = row / N;
 
         // pass 1: Welford of lanes (s0, s1) and (s2, s3), one f32x2 op each
         f2_t m01 = f2(0.f, 0.f), q01 = m01, m23 = m01, q23 = m01;
@@ -115,6 +166,7 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t N, int D,
         // pass 2: normalise, modulate, store
         const uint16_t *scr = scale + b * s_scale_b + c0;
         const uint16_t *shr = shift + b * s_shift_b + c0;
+        const uint32_t *ob = opsh + b * D + c0;  // OPSH: (op, shift) of the column pairs from c0 on
         uint16_t *orow = out + row * (int64_t)D + c0;
         const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
 #pragma unroll
@@ -123,41 +175,63 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t N, int D,
             for (int s = 0; s < 4; ++s) {
                 if (i < NI - 1 || vlast[s]) {
                     const int off = 512 * i + 32 * s;
-                    uint32_t sc[2], sh[2], o[2];
-                    ld_keep8(sc, scr + off);
-                    ld_keep8(sh, shr + off);
+                    uint32_t op[2], sh[2], o[2];
+                    if constexpr (OPSH) {
+                        const uint4 t = *reinterpret_cast<const uint4 *>(ob + off);
+                        op[0] = t.x;
+                        sh[0] = t.y;
+                        op[1] = t.z;
+                        sh[1] = t.w;
+                    } else {
+                        uint32_t sc[2];
+                        ld_keep8(sc, scr + off);
+                        ld_keep8(sh, shr + off);
+                        op[0] = add16x2<T>(sc[0], one16x2<T>());
+                        op[1] = add16x2<T>(sc[1], one16x2<T>());
+                    }
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
                         float xl, xh;
                         unpack_again<T>(xv[i][s][k], xl, xh);
                         float y0, y1;
                         f2_split(f2_mul(f2_sub(f2(xl, xh), mm), rr), y0, y1);
-                        const uint32_t op = add16x2<T>(sc[k], one16x2<T>());
-                        o[k] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0, y1), op), sh[k]);
+                        o[k] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0, y1), op[k]), sh[k]);
                     }
                     st8(orow + off, o);
                 }
             }
         }
+        if (row + kRowsThreads / 32 < r1) {
+            load_row(row + kRowsThreads / 32);
+            prefetch_row(row + 2 * (kRowsThreads / 32));
+        }
     }
     pdl_trigger();
 }
 
-template <DT T, int NI, bool TAIL>
+template <DT T, int NI, bool TAIL, bool OPSH>
 static cudaError_t run_rows(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    auto k = ln_rows_kernel<T, NI, TAIL>;
+    auto k = ln_rows_kernel<T, NI, TAIL, OPSH>;
+    const size_t smem = OPSH ? (size_t)(a.B * a.D * 4) : 0;
     const int64_t rows = a.B * a.N;
     const int64_t ctas_needed = (rows + kRowsThreads / 32 - 1) / (kRowsThreads / 32);
-    const int64_t grid = imin64(ctas_needed, (int64_t)dev.sms * blocks_per_sm(k, kRowsThreads, 0));
-    return launch_k(k, dim3((unsigned)grid), dim3(kRowsThreads), 0, s, pdl, (uint16_t *)a.out,
-                    (const uint16_t *)a.x, rows, a.N, (int)a.D, a.sxB, a.sxN,
+    const int64_t grid = imin64(ctas_needed, (int64_t)dev.sms * blocks_per_sm(k, kRowsThreads, smem));
+    return launch_k(k, dim3((unsigned)grid), dim3(kRowsThreads), smem, s, pdl, (uint16_t *)a.out,
+                    (const uint16_t *)a.x, rows, a.B, a.N, (int)a.D, a.sxB, a.sxN,
                     (const uint16_t *)a.scale, a.s_scale_b, (const uint16_t *)a.shift, a.s_shift_b,
                     a.eps);
 }
 
+// the op / shift table of all samples fits in shared memory (the rows path
+// already guarantees 8-byte aligned scale / shift and even strides)
+static inline bool rows_opsh_ok(const LnArgs &a) { return a.B * a.D * 4 <= kOpshMaxBytes; }
+
 template <DT T, int NI>
 static cudaError_t rows_tail(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    return (a.D % 512 == 0) ? run_rows<T, NI, false>(a, pdl, s, dev) : run_rows<T, NI, true>(a, pdl, s, dev);
+    const bool tail = a.D % 512 != 0;
+    if (rows_opsh_ok(a))
+        return tail ? run_rows<T, NI, true, true>(a, pdl, s, dev) : run_rows<T, NI, false, true>(a, pdl, s, dev);
+    return tail ? run_rows<T, NI, true, false>(a, pdl, s, dev) : run_rows<T, NI, false, false>(a, pdl, s, dev);
 }
 
 template <DT T>

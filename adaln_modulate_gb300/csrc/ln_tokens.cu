@@ -15,10 +15,10 @@ namespace adaln {
 //      visible to both;
 //   2. pass 1: serial Welford of lane l for its 4 tokens, states to shared
 //      memory;
-//   3. warps 0..3 fold the token pair (2w, 2w+1) over the 128 lane states
-//      (4 lanes per thread in the stride-8 mapping of the contiguous-rows
-//      kernel, one f32x2 op covering both tokens, coefficients from the
-//      fold plan) and write mean / rstd;
+//   3. warp w folds token w over its 128 lane states (4 lanes per thread in
+//      the stride-8 mapping of the contiguous-rows kernel, coefficients from
+//      the fold plan); every lane computes the same mean / rstd, lane 0
+//      writes them;
 //   4. pass 2: thread (l, h) normalises its rows for its 4 tokens, applies
 //      the modulate and stores 4 consecutive d of each token (8 bytes).
 // Shared-memory reads of a warp cover 256 contiguous bytes (16 lanes x 2
@@ -28,50 +28,14 @@ namespace adaln {
 constexpr int kTok = 8;
 constexpr int kTokThreads = 256;
 constexpr int kStPitch = 128 + 24;
+static_assert(kTokThreads / 32 == kTok, "one fold warp per token");
 __device__ __forceinline__ int st_idx(int l) { return l + 8 * (l >> 5); }
 
-__device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, int src_bytes) {
-    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // 8-byte shared load (volatile, so the output pass re-reads the tile rather
 // than keeping the statistics pass's values alive)
 __device__ __forceinline__ void lds64_again(uint32_t *r, uint32_t saddr) {
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(saddr));
-}
-
-// butterfly stage across threads on a token pair
-__device__ __forceinline__ void shfl_stage_p2(f2_t &m, f2_t &q, int mask, float coef, float na) {
-    const f2_t pm = __shfl_xor_sync(0xffffffffu, m, mask);
-    const f2_t pq = __shfl_xor_sync(0xffffffffu, q, mask);
-    const bool lower = (threadIdx.x & mask) == 0;
-    const f2_t lo = lower ? m : pm, up = lower ? pm : m;
-    const f2_t delta = f2_sub(up, lo);
-    const f2_t c = f2(coef, coef);
-    m = f2_fma(delta, c, lo);
-    q = f2_fma(f2_mul(f2_mul(delta, delta), f2(na, na)), c, f2_add(q, pq));
-}
-
-// the stride-8 fold of fold128_s8 on two tokens at once: sX holds lane
-// l0 + 8X of the thread for (token a, token b)
-__device__ __forceinline__ void fold128_s8_x2(f2_t m0, f2_t q0, f2_t m1, f2_t q1, f2_t m2, f2_t q2,
-                                              f2_t m3, f2_t q3, const FoldPlan &p, f2_t &mean, f2_t &m2o) {
-    chan_p2(m0, q0, m2, q2, f2(p.c16[0], p.c16[0]), f2(p.n16[0], p.n16[0]));  // offset 16, s0 + s2
-    chan_p2(m1, q1, m3, q3, f2(p.c16[1], p.c16[1]), f2(p.n16[1], p.n16[1]));  // offset 16, s1 + s3
-    chan_p2(m0, q0, m1, q1, f2(p.c8, p.c8), f2(p.n8, p.n8));                  // offset 8
-    shfl_stage_p2(m0, q0, 4, p.c[0], p.n[0]);
-    shfl_stage_p2(m0, q0, 2, p.c[1], p.n[1]);
-    shfl_stage_p2(m0, q0, 1, p.c[2], p.n[2]);
-    shfl_stage_p2(m0, q0, 16, p.c[3], p.n[3]);
-    shfl_stage_p2(m0, q0, 8, p.c[4], p.n[4]);
-    mean = m0;
-    m2o = q0;
 }
 
 template <DT T, int NI>
@@ -95,12 +59,6 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
     const uint32_t tile_s = (uint32_t)__cvta_generic_to_shared(tile);
     // this thread's 8 bytes of the lane-l slot of row group g: tile_s + 16*(g*128 + l) + 8h
     const uint32_t my_s = tile_s + 16 * l + 8 * h;
-    if (tid < 32) {
-        const FoldPlan pl = (D % 512 == 0) ? fold_plan_uniform(NI) : fold_plan_runtime(tid, nvec);
-        const float *f = reinterpret_cast<const float *>(&pl);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) plan_s[k][tid] = f[k];
-    }
     pdl_wait();
 
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -121,6 +79,14 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
                 cp_async16_zfill(&tile[(i * 4 + 2 * h + 1) * 128 + l], src + sxD, 2 * ntok);
             }
             cp_async_commit();
+        }
+        if (t == blockIdx.x && tid < 32) {
+            // fold plan of lane-group u = tid (read by every warp in step 3),
+            // computed while the first copies are in flight
+            const FoldPlan pl = (D % 512 == 0) ? fold_plan_uniform(NI) : fold_plan_runtime(tid, nvec);
+            const float *f = reinterpret_cast<const float *>(&pl);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) plan_s[k][tid] = f[k];
         }
 
         // 2. pass 1: Welford of lane l, tokens 4h .. 4h+3
@@ -161,27 +127,22 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
         }
         __syncthreads();
 
-        // 3. warp w < 4 folds the token pair (2w, 2w + 1)
-        if (warp < kTok / 2) {
+        // 3. warp w folds token w (a token past the end folds zeros, unused)
+        {
             const int u = tid & 31;
             const int i0 = st_idx((u & 7) + 32 * (u >> 3));
-            const float *ma0 = st_mean[2 * warp], *ma1 = st_mean[2 * warp + 1];
-            const float *qa0 = st_m2[2 * warp], *qa1 = st_m2[2 * warp + 1];
+            const float *mw = st_mean[warp], *qw = st_m2[warp];
             FoldPlan plan;
             float *f = reinterpret_cast<float *>(&plan);
 #pragma unroll
             for (int k = 0; k < 16; ++k) f[k] = plan_s[k][u];
-            f2_t mean2, m22;
-            fold128_s8_x2(f2(ma0[i0], ma1[i0]), f2(qa0[i0], qa1[i0]), f2(ma0[i0 + 8], ma1[i0 + 8]),
-                          f2(qa0[i0 + 8], qa1[i0 + 8]), f2(ma0[i0 + 16], ma1[i0 + 16]),
-                          f2(qa0[i0 + 16], qa1[i0 + 16]), f2(ma0[i0 + 24], ma1[i0 + 24]),
-                          f2(qa0[i0 + 24], qa1[i0 + 24]), plan, mean2, m22);
-            if (u < 2) {
-                float mx, my, qx, qy;
-                f2_split(mean2, mx, my);
-                f2_split(m22, qx, qy);
-                fin[0][2 * warp + u] = u ? my : mx;
-                fin[1][2 * warp + u] = finish_rstd(u ? qy : qx, Df, eps);
+            float mean, m2;
+            fold128_s8(f2(mw[i0], mw[i0 + 8]), f2(qw[i0], qw[i0 + 8]), f2(mw[i0 + 16], mw[i0 + 24]),
+                       f2(qw[i0 + 16], qw[i0 + 24]), plan, mean, m2);
+            const float rstd = finish_rstd(m2, Df, eps);
+            if (u == 0) {
+                fin[0][warp] = mean;
+                fin[1][warp] = rstd;
             }
         }
         __syncthreads();

@@ -146,7 +146,7 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
             mean = lm[0];
             m2 = lq[0];
         }
-        const float rstd = rsqrt_cr(__fadd_rn(__fdiv_rn(m2, Df), eps));
+        const float rstd = rsqrt_rn(__fadd_rn(__fdiv_rn(m2, Df), eps));
 
         // out = round(fma(w, rstd * (x - mean), b))
         const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
@@ -181,6 +181,137 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
     pdl_trigger();
 }
 
+// ---------------------------------------------------------------------
+// Dh = 128, two threads per row.  Thread t (= 0, 1) of a row holds the lane
+// pairs (4k + 2t, 4k + 2t + 1), k = 0..7: one 16-byte access per k, and the
+// two threads of a row cover 32 contiguous bytes.  The butterfly: offsets
+// 16, 8, 4 (k bits) inside the thread on f32x2 lane pairs (j = 0, 1),
+// offset 2 (the thread bit) with one shuffle of the pair, offset 1 (j)
+// inside the thread.  A warp takes 16 rows per iteration; the loop is
+// uniform across the warp (threads past the end compute on zeros and store
+// nothing), so every shuffle sees the full warp.
+// ---------------------------------------------------------------------
+
+template <DT T>
+__global__ void __launch_bounds__(kQkThreads)
+qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out,
+                  const uint16_t *k, int64_t rows_k, const uint16_t *wq, const uint16_t *bq,
+                  const uint16_t *wk, const uint16_t *bk, float eps) {
+    __shared__ __align__(16) float aff[2][2][128];  // [q / k][w / b][column]
+    constexpr int NL = 32;
+    pdl_wait();
+    for (int c = threadIdx.x; c < 128; c += kQkThreads) {
+        aff[0][0][c] = rows_q ? h_f32<T>(wq[c]) : 0.0f;
+        aff[0][1][c] = rows_q ? h_f32<T>(bq[c]) : 0.0f;
+        aff[1][0][c] = rows_k ? h_f32<T>(wk[c]) : 0.0f;
+        aff[1][1][c] = rows_k ? h_f32<T>(bk[c]) : 0.0f;
+    }
+    __syncthreads();
+
+    const int t = threadIdx.x & 1;
+    const int64_t total = rows_q + rows_k;
+    const int64_t w0 = (((int64_t)blockIdx.x * kQkThreads + threadIdx.x) >> 5) * 16;
+    const int64_t wstride = ((int64_t)gridDim.x * kQkThreads >> 5) * 16;
+    const int rin = (threadIdx.x & 31) >> 1;  // row of this thread within the warp's 16
+
+    for (int64_t rbase = w0; rbase < total; rbase += wstride) {
+        const int64_t r = rbase + rin;
+        const bool active = r < total;
+        const bool isq = r < rows_q;
+        const uint16_t *src = isq ? q + r * 128 : k + (r - rows_q) * 128;
+        uint16_t *dst = isq ? q_out + r * 128 : k_out + (r - rows_q) * 128;
+        const float *w = aff[isq ? 0 : 1][0];
+        const float *bb = aff[isq ? 0 : 1][1];
+
+        uint32_t v[8][4];  // k: lanes 4k + 2t (v[k][0..1]) and 4k + 2t + 1 (v[k][2..3])
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            if (active) {
+                asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v[kk][0]), "=r"(v[kk][1]), "=r"(v[kk][2]), "=r"(v[kk][3])
+                             : "l"(src + 16 * kk + 8 * t));
+            } else {
+                v[kk][0] = v[kk][1] = v[kk][2] = v[kk][3] = 0u;
+            }
+        }
+
+        // Welford of lane pair (4k + 2t, 4k + 2t + 1), one f32x2 chain per k
+        f2_t m[8], qq[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t *a0 = v[kk], *a1 = v[kk] + 2;
+            m[kk] = qq[kk] = f2(0.f, 0.f);
+            push2(m[kk], qq[kk], f2(lo_f32<T>(a0[0]), lo_f32<T>(a1[0])), Rcp<1>::value);
+            push2(m[kk], qq[kk], f2(hi_f32<T>(a0[0]), hi_f32<T>(a1[0])), Rcp<2>::value);
+            push2(m[kk], qq[kk], f2(lo_f32<T>(a0[1]), lo_f32<T>(a1[1])), Rcp<3>::value);
+            push2(m[kk], qq[kk], f2(hi_f32<T>(a0[1]), hi_f32<T>(a1[1])), Rcp<4>::value);
+        }
+        // offsets 16, 8, 4: k with k + 4, k + 2, k + 1 (all lane counts equal)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            chan_p2(m[kk], qq[kk], m[kk + 4], qq[kk + 4], f2(qk_coef(0, 16, NL), qk_coef(0, 16, NL)),
+                    f2(qk_count(0, 16, NL), qk_count(0, 16, NL)));
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+            chan_p2(m[kk], qq[kk], m[kk + 2], qq[kk + 2], f2(qk_coef(0, 8, NL), qk_coef(0, 8, NL)),
+                    f2(qk_count(0, 8, NL), qk_count(0, 8, NL)));
+        chan_p2(m[0], qq[0], m[1], qq[1], f2(qk_coef(0, 4, NL), qk_coef(0, 4, NL)),
+                f2(qk_count(0, 4, NL), qk_count(0, 4, NL)));
+        {  // offset 2: the partner thread holds lanes with the other t
+            const f2_t pm = __shfl_xor_sync(0xffffffffu, m[0], 1);
+            const f2_t pq = __shfl_xor_sync(0xffffffffu, qq[0], 1);
+            const f2_t lo = t ? pm : m[0], up = t ? m[0] : pm;
+            const f2_t delta = f2_sub(up, lo);
+            const f2_t c2 = f2(qk_coef(0, 2, NL), qk_coef(0, 2, NL));
+            m[0] = f2_fma(delta, c2, lo);
+            qq[0] = f2_fma(f2_mul(f2_mul(delta, delta), f2(qk_count(0, 2, NL), qk_count(0, 2, NL))), c2,
+                           f2_add(qq[0], pq));
+        }
+        float a0, a1, b0, b1;
+        f2_split(m[0], a0, a1);
+        f2_split(qq[0], b0, b1);
+        chan_p(a0, b0, a1, b1, qk_coef(0, 1, NL), qk_count(0, 1, NL));  // offset 1
+        const float rstd = rsqrt_rn(__fadd_rn(__fdiv_rn(b0, 128.0f), eps));
+
+        const f2_t mm = f2(a0, a0), rr = f2(rstd, rstd);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t o[4];
+            const int col = 16 * kk + 8 * t;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // lane 4k + 2t + h: columns col + 4h .. +3
+                const float4 w4 = *reinterpret_cast<const float4 *>(w + col + 4 * h);
+                const float4 b4 = *reinterpret_cast<const float4 *>(bb + col + 4 * h);
+                float x0, x1, x2, x3, y0, y1, y2, y3;
+                unpack_again<T>(v[kk][2 * h], x0, x1);
+                unpack_again<T>(v[kk][2 * h + 1], x2, x3);
+                f2_t u01 = f2_mul(f2_sub(f2(x0, x1), mm), rr);
+                f2_t u23 = f2_mul(f2_sub(f2(x2, x3), mm), rr);
+                u01 = f2_fma(f2(w4.x, w4.y), u01, f2(b4.x, b4.y));
+                u23 = f2_fma(f2(w4.z, w4.w), u23, f2(b4.z, b4.w));
+                f2_split(u01, y0, y1);
+                f2_split(u23, y2, y3);
+                o[2 * h] = pack_rn<T>(y0, y1);
+                o[2 * h + 1] = pack_rn<T>(y2, y3);
+            }
+            if (active) st16(dst + col, o);
+        }
+    }
+    pdl_trigger();
+}
+
+template <DT T>
+static cudaError_t run_qk_pair(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    auto kern = qk_ln_pair_kernel<T>;
+    const int64_t total = a.rows_q + a.rows_k;
+    const int64_t ctas = (total * 2 + kQkThreads - 1) / kQkThreads;
+    const int64_t grid = imin64(ctas, (int64_t)dev.sms * blocks_per_sm(kern, kQkThreads, 0));
+    return launch_k(kern, dim3((unsigned)grid), dim3(kQkThreads), 0, s, pdl, (uint16_t *)a.q_out,
+                    (const uint16_t *)a.q, a.rows_q, (uint16_t *)a.k_out, (const uint16_t *)a.k,
+                    a.rows_k, (const uint16_t *)a.wq, (const uint16_t *)a.bq, (const uint16_t *)a.wk,
+                    (const uint16_t *)a.bk, a.eps);
+}
+
 template <DT T, int NL, bool VEC32>
 static cudaError_t run_qk(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     auto kern = qk_ln_kernel<T, NL, VEC32>;
@@ -197,8 +328,8 @@ static bool al(const void *p, int a) { return p == nullptr || ((uintptr_t)p % (u
 
 template <DT T>
 static cudaError_t qk_dispatch(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    const bool a32 = al(a.q, 32) && al(a.k, 32) && al(a.q_out, 32) && al(a.k_out, 32);
-    if (a.Dh == 128) return a32 ? run_qk<T, 32, true>(a, pdl, s, dev) : run_qk<T, 32, false>(a, pdl, s, dev);
+    const bool a16 = al(a.q, 16) && al(a.k, 16) && al(a.q_out, 16) && al(a.k_out, 16);
+    if (a.Dh == 128) return a16 ? run_qk_pair<T>(a, pdl, s, dev) : run_qk<T, 32, false>(a, pdl, s, dev);
     if (a.Dh == 64) return run_qk<T, 16, false>(a, pdl, s, dev);
     return run_qk<T, 0, false>(a, pdl, s, dev);
 }

@@ -211,3 +211,45 @@ def test_broadcast_scale_and_shift_rows(ad):
     out = ad.ln_modulate(xg, sc, sh, 1e-6)
     _, ref = oracle.ln_modulate(x, B, N, D, (N * D, D, 1), table, D, 0, table, 0, 0, 1e-6)
     assert_bits_equal(host_bits(out).reshape(B * N, D), ref, what="broadcast rows")
+
+
+@pytest.mark.parametrize("D", [512, 2240, 4096])
+def test_rows_path_with_8_byte_aligned_rows(ad, D):
+    # x starts 8 bytes past a 16-byte boundary: the rows kernel's 8-byte
+    # accesses only need 8-byte aligned rows
+    B, N = 2, 40
+    x = synth.normal_bits(D + 21, B * N * D, 0, 1).reshape(B, N, D)
+    table = synth.normal_bits(D + 22, B * 2 * D, 0, 0.1).reshape(B, 2, D)
+    buf = torch.empty(B * N * D + 4, dtype=torch.bfloat16, device="cuda")
+    xv = buf[4:].view(B, N, D)
+    xv.copy_(dev_tensor(x))
+    assert xv.data_ptr() % 16 == 8
+    tg = dev_tensor(table).reshape(-1)
+    sc = torch.as_strided(tg, (B, 1, D), (2 * D, D, 1), D)
+    sh = torch.as_strided(tg, (B, 1, D), (2 * D, D, 1), 0)
+    assert ad.ln_modulate_variant(xv, sc, sh, 1e-6) == "rows"
+    out = ad.ln_modulate(xv, sc, sh, 1e-6)
+    _, ref = oracle.ln_modulate(x, B, N, D, (N * D, D, 1), table, D, 2 * D, table, 0, 2 * D, 1e-6)
+    assert_bits_equal(host_bits(out).reshape(B * N, D), ref, what=f"8-byte aligned rows D={D}")
+
+
+@pytest.mark.parametrize("B,D", [(3, 4096), (9, 1024), (5, 2240)])
+def test_rows_without_the_shared_op_shift_table(ad, B, D):
+    # B * D * 4 bytes above 32 KiB: the output pass reads scale / shift from
+    # global memory instead of the per-CTA table
+    assert B * D * 4 > 32 * 1024
+    N = 24
+    x = synth.normal_bits(D + 31, B * N * D, 0, 1).reshape(B, N, D)
+    table = synth.normal_bits(D + 32, B * 2 * D, 0, 0.1).reshape(B, 2, D)
+    got, ref = run_both(ad, x, B, N, D, (N * D, D, 1), table, D, 0, 2 * D, 1e-6, expect="rows")
+    assert_bits_equal(got, ref, what=f"rows without table B={B} D={D}")
+
+
+def test_rows_many_rows_per_warp(ad):
+    # far more rows than resident warps: every warp handles many rows
+    B, N, D = 1, 20000, 512
+    x = synth.normal_bits(23, B * N * D, 0, 1).reshape(B, N, D)
+    table = synth.normal_bits(24, 2 * D, 0, 0.1).reshape(1, 2, D)
+    got, ref = run_both(ad, x, B, N, D, (N * D, D, 1), table, D, 0, 2 * D, 1e-6, expect="rows",
+                        rows=range(0, B * N, 7))
+    assert_bits_equal(got, ref, what="many rows")
