@@ -35,7 +35,7 @@ FLAG_PDL = 1
 STATUS = {0: "ADALN_OK", 1: "ADALN_E_NULL", 2: "ADALN_E_DTYPE", 3: "ADALN_E_SHAPE",
           4: "ADALN_E_ALIGN", 5: "ADALN_E_STRIDE", 6: "ADALN_E_VALUE", 7: "ADALN_E_OVERLAP",
           8: "ADALN_E_CUDA"}
-VARIANTS = {0: "rows", 1: "tokens", 2: "generic"}
+VARIANTS = {0: "rows", 1: "tokens", 2: "generic", 3: "tokens_tma"}
 
 _P, _I, _F, _U, _INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_uint32, ctypes.c_int
 _SIGS = {
@@ -56,6 +56,7 @@ _SIGS = {
     "adaln_bias_gelu_tanh": ([_P, _P, _P, _I, _I, _INT, _U, _P], _INT),
     "adaln_can_bias_gelu_tanh": ([_P, _P, _P, _I, _I, _INT, _U], _INT),
     "adaln_bias_gelu_tanh_noalloc": ([_P, _P, _P, _I, _I, _INT, _U, _P], _INT),
+    "adaln_tma_wait_timeouts": ([_P], _INT),
 }
 
 
@@ -150,6 +151,13 @@ def ln_modulate(x, scale, shift, eps: float, out=None, flags: int = 0, stream=No
                                 hsb, float(eps), _dtype_code(x), flags, _stream(stream))
     _check(st, "adaln_ln_modulate")
     return out
+
+
+def tma_wait_timeouts() -> int:
+    """Bounded TMA waits that gave up on the current device (diagnostic; 0)."""
+    n = ctypes.c_uint32(0)
+    _check(capi.adaln_tma_wait_timeouts(ctypes.byref(n)), "adaln_tma_wait_timeouts")
+    return n.value
 
 
 def ln_modulate_variant(x, scale, shift, eps: float, out=None) -> str:

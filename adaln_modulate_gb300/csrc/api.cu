@@ -272,7 +272,16 @@ int adaln_ln_modulate_variant(const void *out, const void *x, int64_t B, int64_t
         check_ln(out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps, dtype, flags);
     if (st != ADALN_OK) return -(int)st;
     LnArgs a{(void *)out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps};
-    return ln_modulate_path(a);
+    const int path = ln_modulate_path(a);
+    if (path == LN_PATH_TOKENS) {
+        // the TMA tile kernel needs a device (its shared memory) and the driver
+        int dev;
+        DeviceInfo info;
+        if (current_device(&dev) == ADALN_OK && device_info(dev, &info) == ADALN_OK &&
+            ln_tokens_tma_ready(a, info))
+            return LN_PATH_TOKENS_TMA;
+    }
+    return path;
 }
 
 adaln_status adaln_ln_modulate(void *out, const void *x, int64_t B, int64_t N, int64_t D, int64_t sxB,

@@ -54,11 +54,15 @@ struct GeluArgs {
 };
 
 // Which ln_modulate kernel a call takes (exposed for tests and the bench).
-enum LnPath : int { LN_PATH_ROWS = 0, LN_PATH_TOKENS = 1, LN_PATH_GENERIC = 2 };
+enum LnPath : int { LN_PATH_ROWS = 0, LN_PATH_TOKENS = 1, LN_PATH_GENERIC = 2, LN_PATH_TOKENS_TMA = 3 };
 int ln_modulate_path(const LnArgs &a);
 
 cudaError_t launch_ln_modulate(const LnArgs &a, int dtype, bool pdl, cudaStream_t s,
                                const DeviceInfo &dev);
+// the transposed-view tile kernel fed by tensor-memory-accelerator boxes
+bool ln_tokens_tma_fits(const LnArgs &a, const DeviceInfo &dev);
+bool ln_tokens_tma_ready(const LnArgs &a, const DeviceInfo &dev);
+cudaError_t ln_tokens_tma_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 cudaError_t launch_qk_head_layernorm(const QkArgs &a, int dtype, bool pdl, cudaStream_t s,
                                      const DeviceInfo &dev);
 cudaError_t launch_residual_gate_add(const GateArgs &a, int dtype, bool pdl, cudaStream_t s,

@@ -287,6 +287,10 @@ static cudaError_t run_generic(const LnArgs &a, bool pdl, cudaStream_t s, const 
 }
 
 cudaError_t ln_tokens_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    if (ln_tokens_tma_fits(a, dev)) {
+        const cudaError_t e = ln_tokens_tma_launch(a, dtype, pdl, s, dev);
+        if (e != cudaErrorNotSupported) return e;
+    }
     return dtype == 0 ? tokens_ni<DT::BF16>(a, pdl, s, dev) : tokens_ni<DT::FP16>(a, pdl, s, dev);
 }
 

@@ -74,6 +74,15 @@ const char *adaln_last_cuda_error(void);
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 int adaln_version(void);
 
+/* Diagnostic, not an operation of the pages.  Number of times, on the
+ * current device since the library was loaded, that the transposed-view
+ * ln_modulate kernel gave up waiting for its tensor-memory-accelerator
+ * copies (a bounded wait; the affected tile is then left unwritten).  Stays
+ * 0 unless the hardware fails to complete a copy.  Synchronous (a small
+ * device-to-host read).  count: host pointer, written on ADALN_OK.
+ * Returns ADALN_E_NULL or ADALN_E_CUDA on error. */
+adaln_status adaln_tma_wait_timeouts(uint32_t *count);
+
 /* One-time per-device set-up: queries the device and builds the two
  * 65536-entry GELU tables of adaln_bias_gelu_tanh (2 x 128 KiB of device
  * memory, owned by the library).  Synchronous.  Calling it is optional:
@@ -128,11 +137,15 @@ adaln_status adaln_can_ln_modulate(const void *out, const void *x, int64_t B, in
                                    const void *shift, int64_t s_shift_b,
                                    float eps, int dtype, uint32_t flags);
 
-/* Which kernel adaln_ln_modulate would launch for these arguments (no CUDA
- * call): 0 = contiguous rows (sxD == 1, D <= 4096, 8-byte aligned rows),
+/* Which kernel adaln_ln_modulate would launch for these arguments (no
+ * launch): 0 = contiguous rows (sxD == 1, D <= 4096, 8-byte aligned rows),
  * 1 = contiguous tokens (sxN == 1, the transposed view; D <= 6144, 16-byte
- * aligned d-rows), 2 = general strides.  The numbers are identical on every
- * path.  Returns the negative adaln_status if the arguments are invalid. */
+ * aligned d-rows) through the cp.async tile kernel, 3 = the same view
+ * through 16-token tensor-memory-accelerator tiles (D <= 5120 and a CUDA
+ * driver present: this reads the current device's attributes once and
+ * builds the tensor map on the host), 2 = general strides.  The numbers
+ * are identical on every path.  Returns the negative adaln_status if the
+ * arguments are invalid. */
 int adaln_ln_modulate_variant(const void *out, const void *x, int64_t B, int64_t N,
                               int64_t D, int64_t sxB, int64_t sxN, int64_t sxD,
                               const void *scale, int64_t s_scale_b,

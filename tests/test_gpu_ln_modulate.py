@@ -30,7 +30,9 @@ def run_both(ad, xbase, B, N, D, strides, table, sc_off, sh_off, srow, eps, dtyp
     sc = torch.as_strided(tg, (B, 1, D), (srow, D, 1), sc_off)
     sh = torch.as_strided(tg, (B, 1, D), (srow, D, 1), sh_off)
     if expect:
-        assert ad.ln_modulate_variant(xv, sc, sh, eps) == expect
+        got_variant = ad.ln_modulate_variant(xv, sc, sh, eps)
+        # "tokens": either tile kernel of the transposed view
+        assert got_variant == expect or (expect == "tokens" and got_variant == "tokens_tma"), got_variant
     out = ad.ln_modulate(xv, sc, sh, eps)
     torch.cuda.synchronize()
     ids, ref = oracle.ln_modulate(xbase, B, N, D, strides, table, sc_off, srow, table, sh_off, srow,
@@ -119,6 +121,54 @@ def test_tokens_path_ragged(ad, D, N, dtype):
     got, ref = run_both(ad, x, B, N, D, (D * N, 1, N), table, D, 0, 6 * D, 1e-6, dtype,
                         expect="tokens" if N % 8 == 0 else None)
     assert_bits_equal(got, ref, dtype, f"tokens D={D} N={N}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("B,N,D", [(3, 2056, 2240),   # 387 tiles of 16: several per CTA, ragged last
+                                   (1, 4000, 1024),   # one sample, D % 512 == 0
+                                   (2, 48, 5120),     # the largest D of the 16-token TMA tile
+                                   (2, 16, 5632)])    # past it (if shared memory allows)
+def test_tokens_tiles_many_per_cta(ad, B, N, D, dtype):
+    x = synth.normal_bits(D + 11, B * D * N, 0.25, 1.5, dtype).reshape(B, D, N)
+    table = synth.normal_bits(D + 12, B * 6 * D, 0, 0.1, dtype).reshape(B, 6, D)
+    rows = range(0, B * N, 3) if B * N > 4000 else None
+    got, ref = run_both(ad, x, B, N, D, (D * N, 1, N), table, D, 0, 6 * D, 1e-6, dtype,
+                        expect="tokens", rows=rows)
+    assert_bits_equal(got, ref, dtype, f"tokens tiles B={B} N={N} D={D}")
+    assert ad.tma_wait_timeouts() == 0
+
+
+def test_sana_takes_the_tma_tile_kernel(ad):
+    # the transposed headline shape goes through the 16-token TMA tiles; the
+    # largest D past them through the cp.async tiles
+    B, N, D = 2, 1024, 2240
+    x = synth.normal_bits(35, B * D * N, 0, 1).reshape(B, D, N)
+    table = synth.normal_bits(36, B * 6 * D, 0, 0.1).reshape(B, 6, D)
+    got, ref = run_both(ad, x, B, N, D, (D * N, 1, N), table, D, 0, 6 * D, 1e-6,
+                        expect="tokens_tma", rows=range(0, B * N, 17))
+    assert_bits_equal(got, ref, what="tma tiles")
+    xg = torch.empty((1, 6144, 16), dtype=torch.bfloat16, device="cuda")
+    tg = torch.zeros((1, 2, 6144), dtype=torch.bfloat16, device="cuda")
+    assert ad.ln_modulate_variant(xg.permute(0, 2, 1), tg[:, 1:2], tg[:, 0:1], 1e-6) == "tokens"
+
+
+def test_tokens_pdl_orders_after_producer(ad):
+    B, N, D = 2, 1024, 2240
+    x = synth.normal_bits(33, B * D * N, 0, 1).reshape(B, D, N)
+    table = synth.normal_bits(34, B * 6 * D, 0, 0.1).reshape(B, 6, D)
+    _, ref = oracle.ln_modulate(x, B, N, D, (D * N, 1, N), table, D, 6 * D, table, 0, 6 * D, 1e-6,
+                                threads=THREADS)
+    s = torch.cuda.Stream()
+    xg = torch.zeros((B, D, N), dtype=torch.bfloat16, device="cuda")
+    src = dev_tensor(x)
+    tg = dev_tensor(table)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            xg.copy_(src)           # producer kernel on the same stream
+            out = ad.ln_modulate(xg.permute(0, 2, 1), tg[:, 1:2], tg[:, 0:1], 1e-6, flags=ad.FLAG_PDL)
+            xg.zero_()
+    s.synchronize()
+    assert_bits_equal(host_bits(out).reshape(B * N, D), ref, what="tokens pdl")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
