@@ -8,11 +8,16 @@ shift = chunk 0, eps = 1e-6.  One step = one call of the op on that input.
 value = algorithmic bytes (x read once, out written once, scale / shift rows
 read once) / mean device time per call, in GB/s.
 
-Timing: W untimed warm-up calls, then K timed calls.  Before every call L2
-is flushed (a 256 MiB buffer is written, then another is read, so no dirty
-flush lines are left to write back during the call) and each call is
-bracketed by CUDA events on the launching stream.  Clocks and throttle
-reasons are sampled with nvidia-smi during the timed region.
+Timing: W untimed warm-up steps, then exactly K steps timed as one region
+(synchronised on both sides, CUDA events on the launching stream).  Inputs
+are larger than L2: the op's inputs and output are replicated into R sets
+that together cover at least 4x the L2, and step k uses set k mod R, so no
+step finds its inputs in L2.  The K steps are launched from CUDA graphs,
+each kernel with programmatic dependent launch.  As a diagnostic, the same
+op is also timed one call at a time with L2 flushed before each call (a
+256 MiB buffer written, then another read) and CUDA events around each.
+Clocks and throttle reasons are sampled with nvidia-smi during the timed
+region.
 
 Also reported: e2e (the same metric with the inputs copied host -> device
 from pinned memory and the output copied back inside every timed step), the
@@ -164,64 +169,76 @@ def torch_bits(bits, dtype, dev):
     return t.to(dev)
 
 
-def make_workloads(dev, which):
-    """name -> (callable issuing one op, algorithmic bytes, description)."""
+def make_workloads(dev, which, n_sets=None, flags=0):
+    """name -> (list of callables, each one step of the op on its own copy of
+    the inputs and output, algorithmic bytes per step, description).  n_sets
+    copies rotate so that one pass over them touches at least 4x the L2
+    (n_sets=None), or exactly n_sets copies."""
     import torch
 
     import adaln_modulate_gb300 as ad
     import synth
+
+    def sets_for(nbytes):
+        if n_sets is not None:
+            return n_sets
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        return max(1, -(-4 * l2 // nbytes))
+
+    def copies(ts, k):
+        return [ts] + [[t.clone() for t in ts] for _ in range(k - 1)]
 
     out = {}
     if "sana" in which or "sana_nmod2" in which:
         for nmod in ([6] if "sana" in which else []) + ([2] if "sana_nmod2" in which else []):
             w = synth.ln_sana(nmod=nmod)
             B, N, D = 2, 1024, 2240
-            xb = torch_bits(w.tensors["x"].draw(), "bf16", dev)
-            tb = torch_bits(w.tensors["table"].draw(), "bf16", dev)
-            x = xb.permute(0, 2, 1)
-            sc, sh = tb[:, 1:2], tb[:, 0:1]
-            o = torch.empty((B, N, D), dtype=torch.bfloat16, device=dev)
-            out["sana" if nmod == 6 else "sana_nmod2"] = (
-                lambda x=x, sc=sc, sh=sh, o=o: ad.ln_modulate(x, sc, sh, 1e-6, out=o),
-                ln_bytes(B, N, D), w.name)
+            nb = ln_bytes(B, N, D)
+            base = [torch_bits(w.tensors["x"].draw(), "bf16", dev), torch_bits(w.tensors["table"].draw(), "bf16", dev),
+                    torch.empty((B, N, D), dtype=torch.bfloat16, device=dev)]
+            calls = [(lambda xb=xb, tb=tb, o=o: ad.ln_modulate(xb.permute(0, 2, 1), tb[:, 1:2], tb[:, 0:1], 1e-6,
+                                                                out=o, flags=flags))
+                     for xb, tb, o in copies(base, sets_for(nb))]
+            out["sana" if nmod == 6 else "sana_nmod2"] = (calls, nb, w.name)
     if "tiny" in which:
         w = synth.ln_tiny()
-        x, sc, sh = (torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift"))
-        o = torch.empty_like(x)
-        out["tiny"] = (lambda x=x, sc=sc, sh=sh, o=o: ad.ln_modulate(x, sc, sh, 1e-6, out=o),
-                       ln_bytes(1, 64, 512), w.name)
-    if "glm_ln" in which or "glm_gate" in which:
+        nb = ln_bytes(1, 64, 512)
+        base = [torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift")]
+        base.append(torch.empty_like(base[0]))
+        out["tiny"] = ([(lambda x=x, sc=sc, sh=sh, o=o: ad.ln_modulate(x, sc, sh, 1e-6, out=o, flags=flags))
+                        for x, sc, sh, o in copies(base, sets_for(nb))], nb, w.name)
+    if "glm_ln" in which:
         w = synth.ln_glm()
-        x, sc, sh = (torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift"))
-        o = torch.empty_like(x)
-        if "glm_ln" in which:
-            out["glm_ln"] = (lambda x=x, sc=sc, sh=sh, o=o: ad.ln_modulate(x, sc, sh, 1e-5, out=o),
-                             ln_bytes(1, 4096, 4096), w.name)
-        if "glm_gate" in which:
-            wg = synth.gate_add_glm()
-            y = torch_bits(wg.tensors["y"].draw(), "bf16", dev)
-            g = torch_bits(wg.tensors["gate"].draw(), "bf16", dev)
-            o2 = torch.empty_like(x)
-            out["glm_gate"] = (lambda x=x, g=g, y=y, o2=o2: ad.residual_gate_add(x, g, y, out=o2),
-                               3 * 4096 * 4096 * 2 + 4096 * 2, wg.name)
+        nb = ln_bytes(1, 4096, 4096)
+        base = [torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift")]
+        base.append(torch.empty_like(base[0]))
+        out["glm_ln"] = ([(lambda x=x, sc=sc, sh=sh, o=o: ad.ln_modulate(x, sc, sh, 1e-5, out=o, flags=flags))
+                          for x, sc, sh, o in copies(base, sets_for(nb))], nb, w.name)
+    if "glm_gate" in which:
+        wg = synth.gate_add_glm()
+        nb = 3 * 4096 * 4096 * 2 + 4096 * 2
+        base = [torch_bits(wg.tensors[k].draw(), "bf16", dev) for k in ("x", "gate", "y")]
+        base.append(torch.empty_like(base[0]))
+        out["glm_gate"] = ([(lambda x=x, g=g, y=y, o=o: ad.residual_gate_add(x, g, y, out=o, flags=flags))
+                            for x, g, y, o in copies(base, sets_for(nb))], nb, wg.name)
     if "qk" in which:
         w = synth.qk_glm()
-        q, k = (torch_bits(w.tensors[n].draw(), "bf16", dev) for n in ("q", "k"))
-        ws = [torch_bits(w.tensors[n].draw(), "bf16", dev) for n in ("wq", "bq", "wk", "bk")]
-        qo, ko = torch.empty_like(q), torch.empty_like(k)
         rows = 4360 * 32
-        out["qk"] = (lambda q=q, k=k, ws=ws, qo=qo, ko=ko: ad.qk_head_layernorm(q, k, *ws, 1e-6, q_out=qo,
-                                                                                  k_out=ko),
-                     2 * 2 * rows * 128 * 2 + 4 * 128 * 2, w.name)
+        nb = 2 * 2 * rows * 128 * 2 + 4 * 128 * 2
+        base = [torch_bits(w.tensors[n].draw(), "bf16", dev) for n in ("q", "k", "wq", "bq", "wk", "bk")]
+        base += [torch.empty_like(base[0]), torch.empty_like(base[1])]
+        out["qk"] = ([(lambda t=t: ad.qk_head_layernorm(t[0], t[1], t[2], t[3], t[4], t[5], 1e-6, q_out=t[6],
+                                                       k_out=t[7], flags=flags))
+                      for t in copies(base, sets_for(nb))], nb, w.name)
     for dt in ("bf16", "fp16"):
         key = f"gelu_{dt}"
         if key in which:
             w = synth.gelu_wan(dt)
-            x = torch_bits(w.tensors["x"].draw(dt), dt, dev)
-            b = torch_bits(w.tensors["bias"].draw(dt), dt, dev)
-            o = torch.empty_like(x)
-            out[key] = (lambda x=x, b=b, o=o: ad.bias_gelu_tanh(x, b, out=o),
-                        2 * 32760 * 13824 * 2 + 13824 * 2, w.name)
+            nb = 2 * 32760 * 13824 * 2 + 13824 * 2
+            base = [torch_bits(w.tensors["x"].draw(dt), dt, dev), torch_bits(w.tensors["bias"].draw(dt), dt, dev)]
+            base.append(torch.empty_like(base[0]))
+            out[key] = ([(lambda x=x, b=b, o=o: ad.bias_gelu_tanh(x, b, out=o, flags=flags))
+                         for x, b, o in copies(base, sets_for(nb))], nb, w.name)
     return out
 
 
@@ -262,6 +279,46 @@ def time_calls(fn, steps, warmup, flush, on_begin=None, on_end=None):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def time_block(calls, steps, warmup, on_begin=None, on_end=None):
+    """Exactly `steps` steps timed as one region: step k runs calls[k % R]
+    (R rotating input sets), all launched from CUDA graphs (one graph of the
+    R calls, replayed, and one of the first steps % R calls); synchronised
+    on both sides.  Returns ms per step."""
+    import torch
+    R = len(calls)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graphs = {}
+    with torch.cuda.stream(s):
+        for c in calls:
+            c()
+        s.synchronize()
+        for n in {R, steps % R} - {0}:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for c in calls[:n]:
+                    c()
+            graphs[n] = g
+    torch.cuda.synchronize()
+    full, rest = divmod(steps, R)
+    for k in range(max(1, -(-warmup // R))):
+        graphs[R].replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if on_begin:
+        on_begin()
+    e0.record()
+    for _ in range(full):
+        graphs[R].replay()
+    if rest:
+        graphs[rest].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if on_end:
+        on_end()
+    return e0.elapsed_time(e1) / steps
+
+
 def e2e_sana(dev, steps, warmup):
     """Host-to-host: pinned inputs copied in, op, output copied back."""
     import torch
@@ -290,14 +347,16 @@ def e2e_sana(dev, steps, warmup):
     return statistics.mean(times), h2d, d2h
 
 
-def time_copy(dev, nbytes, steps, warmup, flush):
-    """A same-byte SM copy (torch's elementwise kernel for b = a * 1; a plain
-    copy_ would go to the copy engine instead)."""
+def copy_calls(dev, nbytes):
+    """Same-byte SM copies (torch's elementwise kernel for b = a * 1; a plain
+    copy_ would run on the copy engine instead), rotating like the ops."""
     import torch
     n = nbytes // 2 // 2  # read + write == nbytes
-    a = torch.ones(n, dtype=torch.bfloat16, device=dev)
-    b = torch.empty_like(a)
-    return time_calls(lambda: torch.mul(a, 1, out=b), steps, warmup, flush)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sets = max(1, -(-4 * l2 // nbytes))
+    bufs = [(torch.ones(n, dtype=torch.bfloat16, device=dev), torch.empty(n, dtype=torch.bfloat16, device=dev))
+            for _ in range(sets)]
+    return [(lambda a=a, b=b: torch.mul(a, 1, out=b)) for a, b in bufs]
 
 
 # ------------------------------------------------------------ CPU baseline
@@ -405,9 +464,11 @@ def run_ours(args):
     import adaln_modulate_gb300 as ad
     ad.init(local)
     flush = Flusher(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
-    main = make_workloads(dev, [args.only])[args.only]
-    fn, nbytes, wname = main
+    # the timed workload: rotating input sets, launched with programmatic
+    # dependent launch (each kernel waits for the previous one before reading)
+    calls, nbytes, wname = make_workloads(dev, [args.only], flags=ad.FLAG_PDL)[args.only]
     sampler = ClockSampler(local)
     sampler.start()
 
@@ -417,34 +478,47 @@ def run_ours(args):
             torch.distributed.barrier()
 
     barrier()
-    times = time_calls(fn, args.steps, args.warmup, flush, on_begin=sampler.mark_begin,
-                       on_end=sampler.mark_end)
+    mean_ms = time_block(calls, args.steps, args.warmup, on_begin=sampler.mark_begin, on_end=sampler.mark_end)
     barrier()
     clocks = sampler.stop()
-    mean_ms = statistics.mean(times)
     mean_ms, value = combine_ranks(mean_ms, nbytes, ws, dev)
     per_gpu = nbytes / (mean_ms * 1e-3) / 1e9
+    # diagnostic: one call at a time, L2 flushed before each, CUDA events around each
+    iso = time_calls(calls[0], min(args.steps, 500), 5, flush)
+    iso_sorted = sorted(iso)
     hbm, src = peaks()
     traffic = profiled_traffic(HEADLINE_PROFILE, HEADLINE_SOURCES) if args.only == "sana" else None
     roof = {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(per_gpu / hbm, 4), "traffic": traffic,
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs, burst copy)" if src == "measured"
             else "fallback 6.8 TB/s", "kernel": HEADLINE_KERNEL if args.only == "sana" else args.only,
-            "algorithmic_bytes_per_launch": nbytes}
+            "algorithmic_bytes_per_launch": nbytes,
+            "launch_time_us": round(mean_ms * 1e3, 3)}
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
             "us_per_call": round(mean_ms * 1e3, 3),
-            "us_per_call_p10_p90": [round(1e3 * sorted(times)[len(times) // 10], 3),
-                                    round(1e3 * sorted(times)[(9 * len(times)) // 10], 3)],
+            "isolated_call_us": {"mean": round(1e3 * statistics.mean(iso), 3),
+                                 "median": round(1e3 * statistics.median(iso), 3),
+                                 "p10": round(1e3 * iso_sorted[len(iso) // 10], 3),
+                                 "p90": round(1e3 * iso_sorted[(9 * len(iso)) // 10], 3),
+                                 "how": "one call at a time, L2 flushed before each, CUDA events "
+                                        "around each (includes the event / launch gap)"},
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": wname, "B": 2, "N": 1024, "D": 2240,
                        "layout": "x = transposed view of contiguous (2, 2240, 1024)",
                        "nmod": 6, "scale_chunk": 1, "shift_chunk": 0, "eps": 1e-6,
-                       "l2": "flushed before every timed call (256 MiB written, then 256 MiB read)",
+                       "l2": f"inputs larger than L2: {len(calls)} rotating input/output sets "
+                             f"({len(calls) * nbytes / 2**20:.0f} MiB, >= 4x the {l2 >> 20} MiB L2), "
+                             f"step k uses set k mod {len(calls)}",
+                       "launch": "the K steps replayed from CUDA graphs, programmatic dependent launch",
                        "parallelism": f"replicas x{ws} (rows independent, no exchange)"},
             "roofline": roof, "gpu_launches": args.steps, "clocks": clocks}
+    if args.only != "sana":
+        line["config"] = {"workload": wname, "l2": line["config"]["l2"], "launch": line["config"]["launch"],
+                          "parallelism": line["config"]["parallelism"]}
+        line["metric"] = f"{args.only} GB/s (profiling run; not the headline)"
 
     if rank == 0 and not args.no_e2e:
         e2e_ms, h2d, d2h = e2e_sana(dev, min(args.steps, 300), min(args.warmup, 10))
@@ -455,24 +529,28 @@ def run_ours(args):
                               "per step, CUDA events around the whole step"}
     if rank == 0 and not args.no_per_config:
         names = ["tiny", "sana", "sana_nmod2", "glm_ln", "glm_gate", "qk", "gelu_bf16", "gelu_fp16"]
-        wl = make_workloads(dev, names)
         per = {}
-        steps = max(10, min(args.steps, 200))
+        steps = max(20, min(args.steps, 400))
         for name in names:
-            f, nb, desc = wl[name]
-            t = time_calls(f, steps, 5, flush)
-            tc = time_copy(dev, nb, steps, 5, flush)
-            us, usc = statistics.mean(t) * 1e3, statistics.mean(tc) * 1e3
+            wl = make_workloads(dev, [name], flags=ad.FLAG_PDL)
+            cl, nb, desc = wl[name]
+            ms = time_block(cl, steps, 3)
+            iso = time_calls(cl[0], max(10, min(args.steps, 200)), 5, flush)
+            cc = copy_calls(dev, nb)
+            msc = time_block(cc, steps, 3)
+            us, usc = ms * 1e3, msc * 1e3
             per[name] = {"workload": desc, "us_per_call": round(us, 3),
-                         "us_per_call_median": round(statistics.median(t) * 1e3, 3),
                          "gbs": round(nb / (us * 1e-6) / 1e9, 1),
                          "frac_of_hbm_peak": round(nb / (us * 1e-6) / 1e9 / hbm, 4),
-                         "algorithmic_bytes": nb, "copy_same_bytes_us": round(usc, 3),
-                         "copy_same_bytes_us_median": round(statistics.median(tc) * 1e3, 3),
+                         "algorithmic_bytes": nb, "rotating_sets": len(cl),
+                         "isolated_call_us_median": round(statistics.median(iso) * 1e3, 3),
+                         "copy_same_bytes_us": round(usc, 3),
                          "copy_same_bytes_gbs": round(nb / (usc * 1e-6) / 1e9, 1)}
-            del f
+            del wl, cl, cc
+            torch.cuda.empty_cache()
         line["per_config"] = per
-        line["gpu_launches"] = args.steps  # the headline's timed region; per_config is separate
+        line["per_config_how"] = ("each workload timed like the headline (rotating sets >= 4x L2, CUDA "
+                                  "graphs, PDL) next to a same-byte SM copy timed the same way")
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
