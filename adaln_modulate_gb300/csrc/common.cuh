@@ -199,18 +199,6 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Ask L2 to fetch [p, p + bytes) ahead of the loads that will read it (one
-// bulk request; no registers, no completion to wait for).  p 16-byte
-// aligned, bytes a positive multiple of 16.
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-// the 16-byte aligned part of [p, p + bytes), if any
-__device__ __forceinline__ void prefetch_l2_inner(const void *p, uint64_t bytes) {
-    const uint64_t a = (uint64_t)p, lo = (a + 15) & ~15ull, hi = (a + bytes) & ~15ull;
-    if (hi > lo) prefetch_l2((const void *)lo, (uint32_t)(hi - lo));
-}
-
 // 16 consecutive storage elements (32 bytes) moved with VEC-byte accesses;
 // the caller guarantees VEC-byte alignment.
 template <int VEC> __device__ __forceinline__ void ld16el_stream(uint32_t *r, const uint16_t *p) {

@@ -75,18 +75,8 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
             }
         }
     };
-    // the warp's row after `row`: one L2 prefetch request by lane 0, so that
-    // its DRAM reads overlap this row's work
-    auto prefetch_row = [&](int64_t row) {
-        if (u == 0 && row < r1) {
-            const int64_t b = row / N;
-            prefetch_l2_inner(x + b * sxB + (row - b * N) * sxN, (uint64_t)D * 2);
-        }
-    };
-
     int64_t row = r0 + warp;
     if (row < r1) load_row(row);
-    prefetch_row(row + kRowsThreads / 32);
 
     if constexpr (OPSH) {
         // all loads of a batch in flight before any is used
@@ -201,10 +191,7 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
                 }
             }
         }
-        if (row + kRowsThreads / 32 < r1) {
-            load_row(row + kRowsThreads / 32);
-            prefetch_row(row + 2 * (kRowsThreads / 32));
-        }
+        if (row + kRowsThreads / 32 < r1) load_row(row + kRowsThreads / 32);
     }
     pdl_trigger();
 }

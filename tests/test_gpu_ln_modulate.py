@@ -31,8 +31,8 @@ def run_both(ad, xbase, B, N, D, strides, table, sc_off, sh_off, srow, eps, dtyp
     sh = torch.as_strided(tg, (B, 1, D), (srow, D, 1), sh_off)
     if expect:
         got_variant = ad.ln_modulate_variant(xv, sc, sh, eps)
-        # "tokens": either tile kernel of the transposed view
-        assert got_variant == expect or (expect == "tokens" and got_variant == "tokens_tma"), got_variant
+        # "tokens" / "rows": either kernel of that layout
+        assert got_variant == expect or got_variant == expect + "_tma", got_variant
     out = ad.ln_modulate(xv, sc, sh, eps)
     torch.cuda.synchronize()
     ids, ref = oracle.ln_modulate(xbase, B, N, D, strides, table, sc_off, srow, table, sh_off, srow,
