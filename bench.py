@@ -361,8 +361,20 @@ def copy_calls(dev, nbytes):
 
 # ------------------------------------------------------------ CPU baseline
 
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(budget_s=10.0):
-    """The oracle on the headline workload, on all host cores."""
+    """The oracle on the headline workload: all host cores (rows split over
+    threads), and one core on a bounded sample of rows."""
     import oracle
     import synth
     w = synth.ln_sana()
@@ -378,10 +390,19 @@ def cpu_baseline(budget_s=10.0):
         if el >= budget_s or reps >= 1000:
             break
     per = el / reps
+    # one thread, the first 256 rows, scaled to the workload
+    sample_rows = 256
+    t1 = time.perf_counter()
+    oracle.ln_modulate(x, B, N, D, (D * N, 1, N), table, D, 6 * D, table, 0, 6 * D, 1e-6,
+                       rows=range(sample_rows), threads=1)
+    per1 = (time.perf_counter() - t1) * (B * N) / sample_rows
     return {"value": round(ln_bytes(B, N, D) / per / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle", "seconds_per_call": round(per, 5),
             "sample": f"the full headline workload (2048 rows x 2240), {reps} calls, "
-                      f"{el:.1f} s, rows split over {cores} threads"}
+                      f"{el:.1f} s, rows split over {cores} threads",
+            "single_thread": {"value": round(ln_bytes(B, N, D) / per1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"the first {sample_rows} rows on one thread, scaled to 2048"},
+            "cpu_model": cpu_model()}
 
 
 # ------------------------------------------------------------ arms
