@@ -22,6 +22,9 @@ __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { retur
 // serialisation; it must not read inputs before the preceding grid has
 // completed.  Without the launch attribute both instructions are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream (launched with the attribute) start its
+// CTAs as SMs free up; its own pdl_wait still waits for this whole grid to
+// complete, so every kernel here triggers right after its pdl_wait.
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -197,6 +200,15 @@ __device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, i
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Ask L2 to fetch the 16-byte aligned part of [p, p + bytes) ahead of the
+// loads that will read it: one bulk request, no registers, nothing to wait
+// for.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint64_t bytes) {
+    const uint64_t a = (uint64_t)p, lo = (a + 15) & ~15ull, hi = (a + bytes) & ~15ull;
+    if (hi > lo)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
 }
 
 // 16 consecutive storage elements (32 bytes) moved with VEC-byte accesses;

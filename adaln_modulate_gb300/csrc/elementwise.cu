@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(kEwThreads)
 gate_add_kernel(uint16_t *out, const uint16_t *x, const uint16_t *gate, int64_t s_gate_b,
                 const uint16_t *y, int64_t nvec, int64_t ND, int64_t D) {
     pdl_wait();
+    pdl_trigger();
     constexpr int R = EPT / 2;
     const int64_t stride = (int64_t)gridDim.x * kEwThreads;
     for (int64_t v = (int64_t)blockIdx.x * kEwThreads + threadIdx.x; v < nvec; v += stride) {
@@ -60,7 +61,6 @@ gate_add_kernel(uint16_t *out, const uint16_t *x, const uint16_t *gate, int64_t 
         for (int k = 0; k < R; ++k) o[k] = add16x2<T>(xr[k], mul16x2<T>(gr[k], yr[k]));
         Acc<EPT>::st(out + e0, o);
     }
-    pdl_trigger();
 }
 
 // any D / alignment: one element per thread-iteration in binary32
@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kEwThreads)
 gate_add_scalar_kernel(uint16_t *out, const uint16_t *x, const uint16_t *gate, int64_t s_gate_b,
                        const uint16_t *y, int64_t n, int64_t ND, int64_t D) {
     pdl_wait();
+    pdl_trigger();
     const int64_t stride = (int64_t)gridDim.x * kEwThreads;
     for (int64_t e = (int64_t)blockIdx.x * kEwThreads + threadIdx.x; e < n; e += stride) {
         const int64_t b = e / ND;
@@ -76,7 +77,6 @@ gate_add_scalar_kernel(uint16_t *out, const uint16_t *x, const uint16_t *gate, i
         const float gy = h_f32<T>(to16_rn<T>(__fmul_rn(h_f32<T>(gate[b * s_gate_b + col]), h_f32<T>(y[e]))));
         out[e] = to16_rn<T>(__fadd_rn(h_f32<T>(x[e]), gy));
     }
-    pdl_trigger();
 }
 
 static bool al(const void *p, int a) { return ((uintptr_t)p % (uintptr_t)a) == 0; }
@@ -180,6 +180,7 @@ bias_gelu_kernel(uint16_t *out, const uint16_t *x, const uint16_t *bias, int64_t
         reinterpret_cast<uint4 *>(tab)[i] = reinterpret_cast<const uint4 *>(table)[i];
     __syncthreads();
     pdl_wait();
+    pdl_trigger();
     const int64_t stride = (int64_t)gridDim.x * kGeluThreads;
     for (int64_t v = (int64_t)blockIdx.x * kGeluThreads + threadIdx.x; v < nvec; v += stride) {
         const int64_t e0 = v * EPT;
@@ -191,7 +192,6 @@ bias_gelu_kernel(uint16_t *out, const uint16_t *x, const uint16_t *bias, int64_t
         for (int k = 0; k < R; ++k) o[k] = gelu2<T>(tab, add16x2<T>(xr[k], br[k]));
         Acc<EPT>::st(out + e0, o);
     }
-    pdl_trigger();
 }
 
 template <DT T>
@@ -199,12 +199,12 @@ __global__ void __launch_bounds__(kEwThreads)
 bias_gelu_scalar_kernel(uint16_t *out, const uint16_t *x, const uint16_t *bias, int64_t n,
                         int64_t width, const uint16_t *table) {
     pdl_wait();
+    pdl_trigger();
     const int64_t stride = (int64_t)gridDim.x * kEwThreads;
     for (int64_t e = (int64_t)blockIdx.x * kEwThreads + threadIdx.x; e < n; e += stride) {
         const uint16_t v = to16_rn<T>(__fadd_rn(h_f32<T>(x[e]), h_f32<T>(bias[e % width])));
         out[e] = table[v];
     }
-    pdl_trigger();
 }
 
 template <DT T, int EPT>

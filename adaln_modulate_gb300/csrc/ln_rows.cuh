@@ -34,7 +34,18 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
                int64_t sxB, int64_t sxN, const uint16_t *scale, int64_t s_scale_b,
                const uint16_t *shift, int64_t s_shift_b, float eps) {
     extern __shared__ __align__(16) uint32_t opsh[];  // OPSH: [b][column pair][op, shift]
+    // this CTA's rows, from launch parameters only: computed before waiting
+    // on the previous kernel and passed through shared memory so that the
+    // parameter reads (a constant-cache miss) stay ahead of the wait
+    __shared__ int64_t cta_rows[2];
+    if (threadIdx.x == 0) {
+        const int64_t per = rows / gridDim.x, extra = rows % gridDim.x;
+        cta_rows[0] = blockIdx.x * per + imin64(blockIdx.x, extra);
+        cta_rows[1] = cta_rows[0] + per + (blockIdx.x < extra ? 1 : 0);
+    }
+    __syncthreads();
     pdl_wait();
+    pdl_trigger();
     const int u = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nvec = D >> 2;
@@ -54,9 +65,7 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
 
     // rows are split evenly into contiguous ranges per CTA; warps of the CTA
     // take them round-robin
-    const int64_t per = rows / gridDim.x, extra = rows % gridDim.x;
-    const int64_t r0 = blockIdx.x * per + imin64(blockIdx.x, extra);
-    const int64_t r1 = r0 + per + (blockIdx.x < extra ? 1 : 0);
+    const int64_t r0 = cta_rows[0], r1 = cta_rows[1];
 
     // xv[i][s] = the 4 elements of lane l0 + 8s at step i (2 registers)
     uint32_t xv[NI][4][2];
@@ -149,6 +158,13 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
             });
         });
 
+        // this row has arrived: ask L2 for the warp's next row now, so that
+        // its DRAM reads overlap this row's fold, output pass and stores
+        if (u == 0 && row + kRowsThreads / 32 < r1) {
+            const int64_t rn = row + kRowsThreads / 32, bn = rn / N;
+            prefetch_l2(x + bn * sxB + (rn - bn * N) * sxN, (uint64_t)D * 2);
+        }
+
         float mean, m2;
         fold128_s8(m01, q01, m23, q23, plan, mean, m2);
         const float rstd = finish_rstd(m2, Df, eps);
@@ -193,7 +209,6 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
         }
         if (row + kRowsThreads / 32 < r1) load_row(row + kRowsThreads / 32);
     }
-    pdl_trigger();
 }
 
 template <DT T, int NI, bool TAIL, bool OPSH>

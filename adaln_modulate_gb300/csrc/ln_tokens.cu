@@ -60,6 +60,7 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
     // this thread's 8 bytes of the lane-l slot of row group g: tile_s + 16*(g*128 + l) + 8h
     const uint32_t my_s = tile_s + 16 * l + 8 * h;
     pdl_wait();
+    pdl_trigger();
 
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const int64_t b = t / tiles_per_b;
@@ -183,7 +184,6 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
         }
         __syncthreads();  // the tile, st_* and fin are reused by the next tile
     }
-    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------
@@ -201,6 +201,7 @@ ln_generic_kernel(uint16_t *out, const uint16_t *x, int64_t B, int64_t N, int64_
     const int64_t nvec = D >> 2;
     const float Df = (float)D;
     pdl_wait();
+    pdl_trigger();
     for (int64_t row = blockIdx.x; row < B * N; row += gridDim.x) {
         const int64_t b = row / N, n = row - b * N;
         const uint16_t *xr = x + b * sxB + n * sxN;
@@ -234,7 +235,6 @@ ln_generic_kernel(uint16_t *out, const uint16_t *x, int64_t B, int64_t N, int64_
         }
         __syncthreads();
     }
-    pdl_trigger();
 }
 
 template <DT T, int NI>

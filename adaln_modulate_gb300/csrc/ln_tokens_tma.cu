@@ -99,19 +99,33 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
     const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(&bar[0]);
     const uint32_t my_s = tile_s + (uint32_t)(kTTRowBytes * l + 8 * h);  // (step 0, e 0) of this thread
 
+    // Launch parameters are not data of the previous kernel: read them, fetch
+    // the tensor map's descriptor and set up the barriers before waiting on
+    // that kernel (the first read of a parameter misses the constant cache,
+    // about a microsecond).  The first tile's coordinates go through shared
+    // memory so that the parameter reads stay ahead of the wait.
+    __shared__ int64_t first_tile[2];
     if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
 #pragma unroll
         for (int i = 0; i < NI; ++i) mbar_init(bar_s + 8 * i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\nfence.proxy.async.shared::cta;" ::: "memory");
+        const int64_t b0 = (int64_t)blockIdx.x / tiles_per_b;
+        first_tile[0] = b0;
+        first_tile[1] = ((int64_t)blockIdx.x - b0 * tiles_per_b) * kTT;
     }
     __syncthreads();
     pdl_wait();
+    pdl_trigger();
 
     int64_t table_b = -1;
     uint32_t parity = 0;
+    int64_t b = first_tile[0], n0 = first_tile[1];
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, parity ^= 1u) {
-        const int64_t b = t / tiles_per_b;
-        const int64_t n0 = (t - b * tiles_per_b) * kTT;
+        if (t != blockIdx.x) {
+            b = t / tiles_per_b;
+            n0 = (t - b * tiles_per_b) * kTT;
+        }
 
         if (tid == 0) {
             // the previous tile's shared reads are ordered before these
@@ -256,7 +270,6 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
         }
         __syncthreads();  // the tile, lane states, fin and the table are reused by the next tile
     }
-    pdl_trigger();
 }
 
 namespace {

@@ -51,6 +51,7 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
     const int nl = NL ? NL : (Dh >> 2);
     const float Df = (float)Dh;
     pdl_wait();
+    pdl_trigger();
     for (int c = threadIdx.x; c < 128; c += kQkThreads) {
         const bool in = c < Dh;
         aff[0][0][c] = (in && rows_q) ? h_f32<T>(wq[c]) : 0.0f;
@@ -178,7 +179,6 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
                 if (l < nl) st8(dst + 4 * l, o[l]);
         }
     }
-    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------
@@ -200,6 +200,7 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
     __shared__ __align__(16) float aff[2][2][128];  // [q / k][w / b][column]
     constexpr int NL = 32;
     pdl_wait();
+    pdl_trigger();
     for (int c = threadIdx.x; c < 128; c += kQkThreads) {
         aff[0][0][c] = rows_q ? h_f32<T>(wq[c]) : 0.0f;
         aff[0][1][c] = rows_q ? h_f32<T>(bq[c]) : 0.0f;
@@ -297,7 +298,6 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
             if (active) st16(dst + col, o);
         }
     }
-    pdl_trigger();
 }
 
 template <DT T>
