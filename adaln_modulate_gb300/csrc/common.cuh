@@ -186,12 +186,9 @@ __device__ __forceinline__ void st32(void *p, const uint32_t *r) {
                     "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]) : "memory");
 }
 
-// Asynchronous global -> shared copies of 16 bytes (Ampere-style cp.async,
-// bypassing L1), completed per thread with commit / wait groups.
-__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void *gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gmem) : "memory");
-}
-// the same, copying only src_bytes (<= 16) and zero-filling the rest
+// Asynchronous global -> shared copy of 16 bytes (Ampere-style cp.async,
+// bypassing L1) of which only src_bytes (<= 16) are read and the rest is
+// zero-filled; completed per thread with commit / wait groups.
 __device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, int src_bytes) {
     const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
@@ -209,42 +206,6 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint64_t bytes) {
     const uint64_t a = (uint64_t)p, lo = (a + 15) & ~15ull, hi = (a + bytes) & ~15ull;
     if (hi > lo)
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
-}
-
-// 16 consecutive storage elements (32 bytes) moved with VEC-byte accesses;
-// the caller guarantees VEC-byte alignment.
-template <int VEC> __device__ __forceinline__ void ld16el_stream(uint32_t *r, const uint16_t *p) {
-    if constexpr (VEC == 32) {
-        ld_stream32(r, p);
-    } else if constexpr (VEC == 16) {
-        ld_stream16(r, p);
-        ld_stream16(r + 4, p + 8);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ld_stream8(r + 2 * k, p + 4 * k);
-    }
-}
-template <int VEC> __device__ __forceinline__ void ld16el_keep(uint32_t *r, const uint16_t *p) {
-    if constexpr (VEC == 32) {
-        ld_keep32(r, p);
-    } else if constexpr (VEC == 16) {
-        ld_keep16(r, p);
-        ld_keep16(r + 4, p + 8);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ld_keep8(r + 2 * k, p + 4 * k);
-    }
-}
-template <int VEC> __device__ __forceinline__ void st16el(uint16_t *p, const uint32_t *r) {
-    if constexpr (VEC == 32) {
-        st32(p, r);
-    } else if constexpr (VEC == 16) {
-        st16(p, r);
-        st16(p + 8, r + 4);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) st8(p + 4 * k, r + 2 * k);
-    }
 }
 
 // ------------------------------------------- Welford / Chan statistics
@@ -274,26 +235,6 @@ __device__ __forceinline__ Stat chan(const Stat &a, const Stat &b) {
     o.cnt = n;
     return o;
 }
-
-// The same combine for a pair of independent rows sharing counts (the
-// coefficient is computed once).
-__device__ __forceinline__ void chan2(f2_t &ma, f2_t &qa, float na, f2_t mb, f2_t qb, float nb,
-                                      float &n_out) {
-    float n = __fadd_rn(na, nb);
-    float coef = (n == 0.0f) ? 0.0f : __fdiv_rn(nb, n);
-    f2_t delta = f2_sub(mb, ma);
-    f2_t c2 = f2(coef, coef);
-    f2_t na2 = f2(na, na);
-    ma = f2_fma(delta, c2, ma);
-    f2_t dda = f2_mul(f2_mul(delta, delta), na2);
-    float q0, q1, r0, r1;
-    f2_split(qa, q0, q1);
-    f2_split(qb, r0, r1);
-    f2_t qs = f2(__fadd_rn(q0, r0), __fadd_rn(q1, r1));
-    qa = f2_fma(dda, c2, qs);
-    n_out = n;
-}
-
 // Butterfly stage over a warp lane bit: both partners end with
 // chan(lower, upper).
 __device__ __forceinline__ Stat shfl_stage(const Stat &s, int xor_mask, unsigned mask = 0xffffffffu) {

@@ -33,27 +33,6 @@ __device__ __forceinline__ void push1(Stat &s, float v) {
     s.cnt = c1;
 }
 
-// The 128-lane fold when a warp holds all lanes, 4 per thread (thread u has
-// logical lanes 4u..4u+3 in st[0..3]): offsets 16, 8, 4 are thread xor 4, 2,
-// 1; offsets 2, 1 are inside the thread; offsets 64, 32 are thread xor 16,
-// 8.  Every thread returns the merged state of all 128 lanes.
-__device__ __forceinline__ Stat fold128_k4(Stat *st) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) st[s] = shfl_stage(st[s], 4);
-#pragma unroll
-    for (int s = 0; s < 4; ++s) st[s] = shfl_stage(st[s], 2);
-#pragma unroll
-    for (int s = 0; s < 4; ++s) st[s] = shfl_stage(st[s], 1);
-    Stat f = chan(chan(st[0], st[2]), chan(st[1], st[3]));
-    f = shfl_stage(f, 16);
-    return shfl_stage(f, 8);
-}
-
-// Welford count of logical lane l (of 128) after pass 1: 4 per chunk
-__device__ __forceinline__ float lane_count128(int l, int nvec) {
-    return l < nvec ? 4.0f * (float)((nvec - 1 - l) / 128 + 1) : 0.0f;
-}
-
 // ---------------------------------------------------------------------
 // The fold with the "stride-8" lane mapping: thread u of a warp holds the
 // logical lanes l0 + 8s, s = 0..3, with l0 = (u & 7) + 32 (u >> 3).  The

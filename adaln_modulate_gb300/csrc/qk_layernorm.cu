@@ -41,8 +41,7 @@ __host__ __device__ constexpr float qk_coef(int l, int o, int nl) {
 
 // NL: logical lanes holding data (Dh / 4) as a compile-time constant (all
 // fold coefficients are then constants), or 0 for a run-time Dh.
-// VEC32: rows of 128 elements with 32-byte aligned starts.
-template <DT T, int NL, bool VEC32>
+template <DT T, int NL>
 __global__ void __launch_bounds__(kQkThreads)
 qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out,
              const uint16_t *k, int64_t rows_k, int Dh, const uint16_t *wq, const uint16_t *bq,
@@ -71,17 +70,12 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
         const float *bb = aff[isq ? 0 : 1][1];
 
         uint32_t v[32][2];  // lane l: elements 4l..4l+3
-        if constexpr (VEC32) {
 #pragma unroll
-            for (int g = 0; g < 8; ++g) ld_stream32(&v[4 * g][0], src + 16 * g);
-        } else {
-#pragma unroll
-            for (int l = 0; l < 32; ++l) {
-                if (l < nl) {
-                    ld_stream8(v[l], src + 4 * l);
-                } else {
-                    v[l][0] = v[l][1] = 0u;
-                }
+        for (int l = 0; l < 32; ++l) {
+            if (l < nl) {
+                ld_stream8(v[l], src + 4 * l);
+            } else {
+                v[l][0] = v[l][1] = 0u;
             }
         }
 
@@ -170,14 +164,9 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
                 o[l][1] = pack_rn<T>(y2, y3);
             }
         }
-        if constexpr (VEC32) {
 #pragma unroll
-            for (int g = 0; g < 8; ++g) st32(dst + 16 * g, &o[4 * g][0]);
-        } else {
-#pragma unroll
-            for (int l = 0; l < 32; ++l)
-                if (l < nl) st8(dst + 4 * l, o[l]);
-        }
+        for (int l = 0; l < 32; ++l)
+            if (l < nl) st8(dst + 4 * l, o[l]);
     }
 }
 
@@ -312,9 +301,9 @@ static cudaError_t run_qk_pair(const QkArgs &a, bool pdl, cudaStream_t s, const 
                     (const uint16_t *)a.bk, a.eps);
 }
 
-template <DT T, int NL, bool VEC32>
+template <DT T, int NL>
 static cudaError_t run_qk(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    auto kern = qk_ln_kernel<T, NL, VEC32>;
+    auto kern = qk_ln_kernel<T, NL>;
     const int64_t total = a.rows_q + a.rows_k;
     const int64_t ctas = (total + kQkThreads - 1) / kQkThreads;
     const int64_t grid = imin64(ctas, (int64_t)dev.sms * blocks_per_sm(kern, kQkThreads, 0));
@@ -329,9 +318,9 @@ static bool al(const void *p, int a) { return p == nullptr || ((uintptr_t)p % (u
 template <DT T>
 static cudaError_t qk_dispatch(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     const bool a16 = al(a.q, 16) && al(a.k, 16) && al(a.q_out, 16) && al(a.k_out, 16);
-    if (a.Dh == 128) return a16 ? run_qk_pair<T>(a, pdl, s, dev) : run_qk<T, 32, false>(a, pdl, s, dev);
-    if (a.Dh == 64) return run_qk<T, 16, false>(a, pdl, s, dev);
-    return run_qk<T, 0, false>(a, pdl, s, dev);
+    if (a.Dh == 128) return a16 ? run_qk_pair<T>(a, pdl, s, dev) : run_qk<T, 32>(a, pdl, s, dev);
+    if (a.Dh == 64) return run_qk<T, 16>(a, pdl, s, dev);
+    return run_qk<T, 0>(a, pdl, s, dev);
 }
 
 cudaError_t launch_qk_head_layernorm(const QkArgs &a, int dtype, bool pdl, cudaStream_t s,
