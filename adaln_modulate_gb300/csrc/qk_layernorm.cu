@@ -236,6 +236,14 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
             push2(m[kk], qq[kk], f2(lo_f32<T>(a0[1]), lo_f32<T>(a1[1])), Rcp<3>::value);
             push2(m[kk], qq[kk], f2(hi_f32<T>(a0[1]), hi_f32<T>(a1[1])), Rcp<4>::value);
         }
+        // these rows have arrived: ask L2 for the warp's next 16 rows now, so
+        // that their DRAM reads overlap this iteration's fold and stores
+        if ((threadIdx.x & 31) == 0 && rbase + wstride < total) {
+            const int64_t nb = rbase + wstride, ne = imin64(nb + 16, total);
+            if (nb < rows_q) prefetch_l2(q + nb * 128, (uint64_t)(imin64(ne, rows_q) - nb) * 256);
+            const int64_t ks = nb > rows_q ? nb : rows_q;
+            if (ne > ks) prefetch_l2(k + (ks - rows_q) * 128, (uint64_t)(ne - ks) * 256);
+        }
         // offsets 16, 8, 4: k with k + 4, k + 2, k + 1 (all lane counts equal)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
