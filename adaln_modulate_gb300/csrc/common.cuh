@@ -173,15 +173,17 @@ __device__ __forceinline__ void ld_keep32(uint32_t *r, const void *p) {
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]),
           "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]) : "l"(p));
 }
+// Output stores of 8/16/32 bytes, not allocated in L1 (no kernel here reads
+// its output back).
 __device__ __forceinline__ void st8(void *p, const uint32_t *r) {
-    asm volatile("st.global.v2.b32 [%0], {%1, %2};" :: "l"(p), "r"(r[0]), "r"(r[1]) : "memory");
+    asm volatile("st.global.L1::no_allocate.v2.b32 [%0], {%1, %2};" :: "l"(p), "r"(r[0]), "r"(r[1]) : "memory");
 }
 __device__ __forceinline__ void st16(void *p, const uint32_t *r) {
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};"
+    asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1, %2, %3, %4};"
                  :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]) : "memory");
 }
 __device__ __forceinline__ void st32(void *p, const uint32_t *r) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+    asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                  :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
                     "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]) : "memory");
 }
