@@ -1,0 +1,101 @@
+"""All four ops chained on one stream with programmatic dependent launch:
+each op reads what the op before it wrote, so a kernel that read its input
+before its producer finished would return wrong bits.  Every kernel lets its
+dependents launch right after its own wait; the chain runs eagerly and as a
+replayed CUDA graph, and every stage is compared with the same chain on the
+oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import THREADS, assert_bits_equal, dev_tensor, host_bits
+
+pytestmark = pytest.mark.gpu
+
+B, N, D, DH = 1, 512, 2048, 128
+
+
+@pytest.fixture(scope="module")
+def ad():
+    import adaln_modulate_gb300
+    assert torch.cuda.is_available()
+    return adaln_modulate_gb300
+
+
+@pytest.fixture(scope="module")
+def chain_ref():
+    x = synth.normal_bits(51, N * D, 0, 1).reshape(N, D)
+    bias = synth.normal_bits(52, D, 0, 0.02)
+    y = synth.normal_bits(53, N * D, 0, 1).reshape(N, D)
+    gsc = synth.normal_bits(54, 3 * D, 0, 0.1)            # gate, scale, shift rows
+    wq = synth.normal_bits(55, DH, 1.0, 0.05)
+    bq = synth.normal_bits(56, DH, 0.0, 0.05)
+    g = oracle.bias_gelu_tanh(x, bias, N, D, threads=THREADS)[1]
+    r = oracle.residual_gate_add(g, gsc, 0, 0, y, B, N, D, threads=THREADS)[1]
+    ln = oracle.ln_modulate(r, B, N, D, (N * D, D, 1), gsc, D, 0, gsc, 2 * D, 0, 1e-6,
+                            threads=THREADS)[1]
+    qk = oracle.qk_head_layernorm(ln, DH, wq, bq, 1e-6, threads=THREADS)[1]
+    # r read as the transposed view of a contiguous (1, 512, 2048) tensor:
+    # 2048 tokens of 512 channels (the TMA tile kernel)
+    lt = oracle.ln_modulate(r, 1, D, N, (N * D, 1, D), gsc, N, 0, gsc, 2 * N, 0, 1e-6,
+                            threads=THREADS)[1]
+    return dict(x=x, bias=bias, y=y, gsc=gsc, wq=wq, bq=bq, g=g, r=r, ln=ln, qk=qk, lt=lt)
+
+
+def _chain(ad, t):
+    pdl = ad.FLAG_PDL
+    ad.bias_gelu_tanh(t["x"], t["bias"], out=t["g"], flags=pdl)
+    rows = t["gsc"].view(3, 1, D)                       # gate, scale, shift as (1, D) rows
+    ad.residual_gate_add(t["g"].view(B, N, D), rows[0], t["y"].view(B, N, D),
+                         out=t["r"].view(B, N, D), flags=pdl)
+    ad.ln_modulate(t["r"].view(B, N, D), rows[1], rows[2], 1e-6, out=t["ln"].view(B, N, D),
+                   flags=pdl)
+    ad.qk_head_layernorm(t["ln"].view(-1, DH), None, t["wq"], t["bq"], t["wq"], t["bq"], 1e-6,
+                         q_out=t["qk"].view(-1, DH), flags=pdl)
+    flat = t["gsc"].view(-1)
+    ad.ln_modulate(t["r"].view(1, N, D).permute(0, 2, 1), flat[N:2 * N].view(1, N),
+                   flat[2 * N:3 * N].view(1, N), 1e-6, out=t["lt"].view(1, D, N), flags=pdl)
+
+
+def _tensors(ref):
+    t = {k: dev_tensor(ref[k]) for k in ("x", "bias", "y", "gsc", "wq", "bq")}
+    for k in ("g", "r", "ln", "qk", "lt"):
+        t[k] = torch.zeros((N, D), dtype=torch.bfloat16, device="cuda")
+    return t
+
+
+def _check(t, ref, what):
+    torch.cuda.synchronize()
+    for k in ("g", "r", "ln", "qk", "lt"):
+        assert_bits_equal(host_bits(t[k]).reshape(-1), ref[k].reshape(-1), what=f"{what}: {k}")
+
+
+def test_chain_eager(ad, chain_ref):
+    t = _tensors(chain_ref)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            for k in ("g", "r", "ln", "qk", "lt"):
+                t[k].zero_()          # a plain kernel between the chains
+            _chain(ad, t)
+    s.synchronize()
+    _check(t, chain_ref, "eager chain")
+
+
+def test_chain_in_a_graph(ad, chain_ref):
+    ad.init(torch.cuda.current_device())   # GELU tables built before capture
+    t = _tensors(chain_ref)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        _chain(ad, t)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for k in ("g", "r", "ln", "qk", "lt"):
+                t[k].zero_()
+            _chain(ad, t)
+    for _ in range(3):
+        g.replay()
+    _check(t, chain_ref, "graph chain")
