@@ -57,6 +57,10 @@ _SIGS = {
     "adaln_can_bias_gelu_tanh": ([_P, _P, _P, _I, _I, _INT, _U], _INT),
     "adaln_bias_gelu_tanh_noalloc": ([_P, _P, _P, _I, _I, _INT, _U, _P], _INT),
     "adaln_tma_wait_timeouts": ([_P], _INT),
+    "adaln_residual_gate_ln_modulate": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U, _P],
+                                        _INT),
+    "adaln_can_residual_gate_ln_modulate": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U],
+                                            _INT),
 }
 
 
@@ -212,6 +216,33 @@ def residual_gate_add(x, gate, y, out=None, flags: int = 0, stream=None):
                                       _dtype_code(x), flags, _stream(stream))
     _check(st, "adaln_residual_gate_add")
     return out
+
+
+def residual_gate_ln_modulate(x, gate, y, scale, shift, eps: float, r_out=None, out=None, flags: int = 0,
+                              stream=None):
+    """``r = x + gate * y`` and ``LN(r) * (1 + scale) + shift`` in one pass for
+    contiguous x, y (B, N, D); gate / scale / shift (B, 1, D) or (B, D) rows.
+    Pass ``r_out=x`` for an in-place residual update.  Returns (r, out)."""
+    torch = _torch()
+    B, N, D = x.shape
+    if not (x.is_contiguous() and y.is_contiguous()) or y.shape != x.shape:
+        raise ValueError("x and y must be contiguous (B, N, D)")
+    if r_out is None:
+        r_out = torch.empty_like(x)
+    if out is None:
+        out = torch.empty_like(x)
+    rows = []
+    for t, name in ((gate, "gate"), (scale, "scale"), (shift, "shift")):
+        p, sb = _rows_view(t, D, name)
+        if t.shape[0] not in (1, B):
+            raise ValueError(f"{name} batch must be 1 or B")
+        rows.append((p, 0 if t.shape[0] == 1 else sb))
+    (gp, gsb), (sp, ssb), (hp, hsb) = rows
+    st = capi.adaln_residual_gate_ln_modulate(r_out.data_ptr(), out.data_ptr(), x.data_ptr(), gp, gsb,
+                                              y.data_ptr(), B, N, D, sp, ssb, hp, hsb, float(eps),
+                                              _dtype_code(x), flags, _stream(stream))
+    _check(st, "adaln_residual_gate_ln_modulate")
+    return r_out, out
 
 
 def bias_gelu_tanh(x, bias, out=None, flags: int = 0, stream=None):

@@ -164,6 +164,25 @@ adaln_status check_gate(const void *out, const void *x, const void *gate, int64_
     return ADALN_OK;
 }
 
+// r_out = x + gate * y and out = LN(r_out) * (1 + scale) + shift, all (B, N, D) contiguous
+adaln_status check_residual_ln(const void *r_out, const void *out, const void *x, const void *gate, int64_t s_gate_b,
+                               const void *y, int64_t B, int64_t N, int64_t D, const void *scale,
+                               int64_t s_scale_b, const void *shift, int64_t s_shift_b, float eps, int dtype,
+                               uint32_t flags) {
+    adaln_status st = check_gate(r_out, x, gate, s_gate_b, y, B, N, D, dtype, flags);
+    if (st != ADALN_OK) return st;
+    st = check_ln(out, r_out, B, N, D, N * D, D, 1, scale, s_scale_b, shift, s_shift_b, eps, dtype, flags);
+    if (st != ADALN_OK) return st;
+    const int64_t nb = 2 * B * N * D;
+    if (overlap(out, nb, r_out, nb) || overlap(out, nb, x, nb) || overlap(out, nb, y, nb) ||
+        overlap(out, nb, gate, 2 * ((B - 1) * s_gate_b + D)))
+        return ADALN_E_OVERLAP;
+    if (overlap(r_out, nb, scale, 2 * ((B - 1) * s_scale_b + D)) ||
+        overlap(r_out, nb, shift, 2 * ((B - 1) * s_shift_b + D)))
+        return ADALN_E_OVERLAP;
+    return ADALN_OK;
+}
+
 adaln_status check_gelu(const void *out, const void *x, const void *bias, int64_t rows, int64_t width,
                         int dtype, uint32_t flags) {
     if (dtype != ADALN_BF16 && dtype != ADALN_FP16) return ADALN_E_DTYPE;
@@ -297,6 +316,30 @@ adaln_status adaln_ln_modulate(void *out, const void *x, int64_t B, int64_t N, i
     LnArgs a{out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps};
     return finish_launch(
         launch_ln_modulate(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+adaln_status adaln_can_residual_gate_ln_modulate(const void *r_out, const void *out, const void *x,
+                                                 const void *gate, int64_t s_gate_b, const void *y, int64_t B,
+                                                 int64_t N, int64_t D, const void *scale, int64_t s_scale_b,
+                                                 const void *shift, int64_t s_shift_b, float eps, int dtype,
+                                                 uint32_t flags) {
+    return check_residual_ln(r_out, out, x, gate, s_gate_b, y, B, N, D, scale, s_scale_b, shift, s_shift_b, eps,
+                             dtype, flags);
+}
+
+adaln_status adaln_residual_gate_ln_modulate(void *r_out, void *out, const void *x, const void *gate,
+                                             int64_t s_gate_b, const void *y, int64_t B, int64_t N, int64_t D,
+                                             const void *scale, int64_t s_scale_b, const void *shift,
+                                             int64_t s_shift_b, float eps, int dtype, uint32_t flags, void *stream) {
+    adaln_status st = check_residual_ln(r_out, out, x, gate, s_gate_b, y, B, N, D, scale, s_scale_b, shift,
+                                        s_shift_b, eps, dtype, flags);
+    if (st != ADALN_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
+    LnArgs a{out, x, B, N, D, N * D, D, 1, scale, s_scale_b, shift, s_shift_b, eps};
+    return finish_launch(launch_residual_gate_ln_modulate(a, y, gate, s_gate_b, r_out, dtype,
+                                                          (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
 }
 
 adaln_status adaln_can_qk_head_layernorm(const void *q_out, const void *q, int64_t rows_q, const void *k_out,

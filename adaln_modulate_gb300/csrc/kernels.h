@@ -67,6 +67,10 @@ cudaError_t launch_qk_head_layernorm(const QkArgs &a, int dtype, bool pdl, cudaS
                                      const DeviceInfo &dev);
 cudaError_t launch_residual_gate_add(const GateArgs &a, int dtype, bool pdl, cudaStream_t s,
                                      const DeviceInfo &dev);
+// r = x + gate * y, out = LN(r) * (1 + scale) + shift; a.x is x (contiguous)
+bool residual_ln_fused_ok(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b, const void *r_out);
+cudaError_t launch_residual_gate_ln_modulate(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b,
+                                             void *r_out, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 cudaError_t launch_bias_gelu_tanh(const GeluArgs &a, int dtype, bool pdl, cudaStream_t s,
                                   const DeviceInfo &dev);
 cudaError_t launch_gelu_table_init(void *table, int dtype, cudaStream_t s);

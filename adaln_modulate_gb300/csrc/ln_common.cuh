@@ -180,6 +180,11 @@ constexpr int kRowsMaxNI = 8;     // contiguous rows in registers: D <= 4096
 constexpr int kTokensMaxNI = 12;  // tokens tile in shared memory: D <= 6144
 cudaError_t ln_rows_bf16(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 cudaError_t ln_rows_fp16(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev);
+// residual gate-add fused in front of the LayerNorm (x, y, r_out, out contiguous)
+cudaError_t ln_rows_gate_bf16(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b, void *r_out,
+                              bool pdl, cudaStream_t s, const DeviceInfo &dev);
+cudaError_t ln_rows_gate_fp16(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b, void *r_out,
+                              bool pdl, cudaStream_t s, const DeviceInfo &dev);
 cudaError_t ln_tokens_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 cudaError_t ln_generic_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 

@@ -54,4 +54,25 @@ cudaError_t launch_ln_modulate(const LnArgs &a, int dtype, bool pdl, cudaStream_
     }
 }
 
+// The fused kernel when the rows path takes these rows and y, r_out and the
+// gate rows are 8-byte aligned with strides that keep them so; otherwise the
+// gate-add kernel writes r and the LayerNorm reads it back (two launches).
+bool residual_ln_fused_ok(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b, const void *r_out) {
+    return ln_modulate_path(a) == LN_PATH_ROWS && ln_aligned(y, 8) && ln_aligned(r_out, 8) && ln_aligned(gate, 8) &&
+           (a.B == 1 || ln_mult(s_gate_b, 4));
+}
+
+cudaError_t launch_residual_gate_ln_modulate(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b,
+                                             void *r_out, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    if (residual_ln_fused_ok(a, y, gate, s_gate_b, r_out))
+        return dtype == 0 ? ln_rows_gate_bf16(a, y, gate, s_gate_b, r_out, pdl, s, dev)
+                          : ln_rows_gate_fp16(a, y, gate, s_gate_b, r_out, pdl, s, dev);
+    const GateArgs g{r_out, a.x, gate, s_gate_b, y, a.B, a.N, a.D};
+    cudaError_t e = launch_residual_gate_add(g, dtype, pdl, s, dev);
+    if (e != cudaSuccess) return e;
+    LnArgs ln = a;
+    ln.x = r_out;
+    return launch_ln_modulate(ln, dtype, pdl, s, dev);
+}
+
 }  // namespace adaln

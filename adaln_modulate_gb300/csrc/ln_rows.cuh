@@ -28,12 +28,24 @@ constexpr int kRowsThreads = 256;
 // read from global memory (L2) in the output pass.
 constexpr int kOpshMaxBytes = 32 * 1024;
 
-template <DT T, int NI, bool TAIL, bool OPSH>
+// GATE: the row is first r = round(x + round(gate * y)) (the residual
+// gate-add chain, x and y contiguous), written to r_out, and the LayerNorm
+// and modulate run on r: one read of x and y, one write of r and out.
+// With OPSH the gate rows join the shared table (after the op / shift
+// pairs, B * D * 2 more bytes).
+struct RowsGate {
+    const uint16_t *y;
+    const uint16_t *gate;
+    int64_t s_gate_b;
+    uint16_t *r_out;
+};
+
+template <DT T, int NI, bool TAIL, bool OPSH, bool GATE>
 __global__ void __launch_bounds__(kRowsThreads, 2)
 ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_t N, int D,
                int64_t sxB, int64_t sxN, const uint16_t *scale, int64_t s_scale_b,
-               const uint16_t *shift, int64_t s_shift_b, float eps) {
-    extern __shared__ __align__(16) uint32_t opsh[];  // OPSH: [b][column pair][op, shift]
+               const uint16_t *shift, int64_t s_shift_b, float eps, RowsGate g) {
+    extern __shared__ __align__(16) uint32_t opsh[];  // OPSH: [b][column pair][op, shift] (+ GATE: [b][pair] gate)
     // this CTA's rows, from launch parameters only: computed before waiting
     // on the previous kernel and passed through shared memory so that the
     // parameter reads (a constant-cache miss) stay ahead of the wait
@@ -92,7 +104,7 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
         constexpr int kFill = 8;
         const int half = D / 2, npairs = (int)B * half;  // npairs <= kOpshMaxBytes / 8
         for (int base = 0; base < npairs; base += kFill * kRowsThreads) {
-            uint32_t s2[kFill], h2[kFill];
+            uint32_t s2[kFill], h2[kFill], g2[kFill];
 #pragma unroll
             for (int k = 0; k < kFill; ++k) {
                 const int e = base + k * kRowsThreads + threadIdx.x;
@@ -100,6 +112,8 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
                     const int bb = e / half, cp = e - bb * half;
                     asm("ld.global.nc.b32 %0, [%1];" : "=r"(s2[k]) : "l"(scale + bb * s_scale_b + 2 * cp));
                     asm("ld.global.nc.b32 %0, [%1];" : "=r"(h2[k]) : "l"(shift + bb * s_shift_b + 2 * cp));
+                    if constexpr (GATE)
+                        asm("ld.global.nc.b32 %0, [%1];" : "=r"(g2[k]) : "l"(g.gate + bb * g.s_gate_b + 2 * cp));
                 }
             }
 #pragma unroll
@@ -108,6 +122,7 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
                 if (e < npairs) {
                     opsh[2 * e] = add16x2<T>(s2[k], one16x2<T>());
                     opsh[2 * e + 1] = h2[k];
+                    if constexpr (GATE) opsh[2 * npairs + e] = g2[k];
                 }
             }
         }
@@ -121,6 +136,29 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
         f2_t m01 = f2(0.f, 0.f), q01 = m01, m23 = m01, q23 = m01;
         static_for<0, NI>([&](auto I) {
             constexpr int i = decltype(I)::value;
+            if constexpr (GATE) {
+                // this step's chunks become r = round(x + round(gate * y)), stored
+                const uint16_t *yr = g.y + row * (int64_t)D + c0;
+                uint16_t *rr_out = g.r_out + row * (int64_t)D + c0;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    if (i < NI - 1 || vlast[s]) {
+                        const int off = 512 * i + 32 * s;
+                        uint32_t yv[2], gv[2];
+                        ld_stream8(yv, yr + off);
+                        if constexpr (OPSH) {
+                            const uint2 t = *reinterpret_cast<const uint2 *>(opsh + 2 * (int)(B * (D / 2)) + b * (D / 2) + (c0 + off) / 2);
+                            gv[0] = t.x;
+                            gv[1] = t.y;
+                        } else {
+                            ld_keep8(gv, g.gate + b * g.s_gate_b + c0 + off);
+                        }
+                        xv[i][s][0] = add16x2<T>(xv[i][s][0], mul16x2<T>(gv[0], yv[0]));
+                        xv[i][s][1] = add16x2<T>(xv[i][s][1], mul16x2<T>(gv[1], yv[1]));
+                        st8(rr_out + off, xv[i][s]);
+                    }
+                }
+            }
             static_for<0, 4>([&](auto E) {
                 constexpr int e = decltype(E)::value;
                 constexpr float r = Rcp<4 * i + e + 1>::value;
@@ -211,42 +249,45 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
     }
 }
 
-template <DT T, int NI, bool TAIL, bool OPSH>
-static cudaError_t run_rows(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    auto k = ln_rows_kernel<T, NI, TAIL, OPSH>;
-    const size_t smem = OPSH ? (size_t)(a.B * a.D * 4) : 0;
+template <DT T, int NI, bool TAIL, bool OPSH, bool GATE>
+static cudaError_t run_rows(const LnArgs &a, const RowsGate &g, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    auto k = ln_rows_kernel<T, NI, TAIL, OPSH, GATE>;
+    // <= 48 KiB (B D 4 <= 32 KiB when OPSH): no opt-in needed
+    const size_t smem = OPSH ? (size_t)(a.B * a.D * (GATE ? 6 : 4)) : 0;
     const int64_t rows = a.B * a.N;
     const int64_t ctas_needed = (rows + kRowsThreads / 32 - 1) / (kRowsThreads / 32);
     const int64_t grid = imin64(ctas_needed, (int64_t)dev.sms * blocks_per_sm(k, kRowsThreads, smem));
     return launch_k(k, dim3((unsigned)grid), dim3(kRowsThreads), smem, s, pdl, (uint16_t *)a.out,
                     (const uint16_t *)a.x, rows, a.B, a.N, (int)a.D, a.sxB, a.sxN,
                     (const uint16_t *)a.scale, a.s_scale_b, (const uint16_t *)a.shift, a.s_shift_b,
-                    a.eps);
+                    a.eps, g);
 }
 
 // the op / shift table of all samples fits in shared memory (the rows path
 // already guarantees 8-byte aligned scale / shift and even strides)
 static inline bool rows_opsh_ok(const LnArgs &a) { return a.B * a.D * 4 <= kOpshMaxBytes; }
 
-template <DT T, int NI>
-static cudaError_t rows_tail(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+template <DT T, int NI, bool GATE>
+static cudaError_t rows_tail(const LnArgs &a, const RowsGate &g, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     const bool tail = a.D % 512 != 0;
     if (rows_opsh_ok(a))
-        return tail ? run_rows<T, NI, true, true>(a, pdl, s, dev) : run_rows<T, NI, false, true>(a, pdl, s, dev);
-    return tail ? run_rows<T, NI, true, false>(a, pdl, s, dev) : run_rows<T, NI, false, false>(a, pdl, s, dev);
+        return tail ? run_rows<T, NI, true, true, GATE>(a, g, pdl, s, dev)
+                    : run_rows<T, NI, false, true, GATE>(a, g, pdl, s, dev);
+    return tail ? run_rows<T, NI, true, false, GATE>(a, g, pdl, s, dev)
+                : run_rows<T, NI, false, false, GATE>(a, g, pdl, s, dev);
 }
 
-template <DT T>
-static cudaError_t rows_vec(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+template <DT T, bool GATE>
+static cudaError_t rows_vec(const LnArgs &a, const RowsGate &g, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     switch ((a.D + 511) / 512) {
-        case 1: return rows_tail<T, 1>(a, pdl, s, dev);
-        case 2: return rows_tail<T, 2>(a, pdl, s, dev);
-        case 3: return rows_tail<T, 3>(a, pdl, s, dev);
-        case 4: return rows_tail<T, 4>(a, pdl, s, dev);
-        case 5: return rows_tail<T, 5>(a, pdl, s, dev);
-        case 6: return rows_tail<T, 6>(a, pdl, s, dev);
-        case 7: return rows_tail<T, 7>(a, pdl, s, dev);
-        case 8: return rows_tail<T, 8>(a, pdl, s, dev);
+        case 1: return rows_tail<T, 1, GATE>(a, g, pdl, s, dev);
+        case 2: return rows_tail<T, 2, GATE>(a, g, pdl, s, dev);
+        case 3: return rows_tail<T, 3, GATE>(a, g, pdl, s, dev);
+        case 4: return rows_tail<T, 4, GATE>(a, g, pdl, s, dev);
+        case 5: return rows_tail<T, 5, GATE>(a, g, pdl, s, dev);
+        case 6: return rows_tail<T, 6, GATE>(a, g, pdl, s, dev);
+        case 7: return rows_tail<T, 7, GATE>(a, g, pdl, s, dev);
+        case 8: return rows_tail<T, 8, GATE>(a, g, pdl, s, dev);
     }
     return cudaErrorInvalidValue;
 }

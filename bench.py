@@ -223,6 +223,17 @@ def make_workloads(dev, which, n_sets=None, flags=0):
         base.append(torch.empty_like(base[0]))
         out["glm_gate"] = ([(lambda x=x, g=g, y=y, o=o: ad.residual_gate_add(x, g, y, out=o, flags=flags))
                             for x, g, y, o in copies(base, sets_for(nb))], nb, wg.name)
+    if "glm_gate_ln" in which:
+        wg, wl = synth.gate_add_glm(), synth.ln_glm()
+        nb = 4 * 4096 * 4096 * 2 + 3 * 4096 * 2  # x, y read; r, out written; gate, scale, shift rows
+        base = [torch_bits(wg.tensors[k].draw(), "bf16", dev) for k in ("x", "gate", "y")]
+        base += [torch_bits(wl.tensors[k].draw(), "bf16", dev) for k in ("scale", "shift")]
+        base += [torch.empty_like(base[0]), torch.empty_like(base[0])]
+        out["glm_gate_ln"] = ([(lambda t=t: ad.residual_gate_ln_modulate(t[0], t[1], t[2], t[3], t[4], 1e-5,
+                                                                         r_out=t[5], out=t[6], flags=flags))
+                               for t in copies(base, sets_for(nb))], nb,
+                              "residual_gate_ln_modulate GLM-Image (1,4096,4096): r = x + gate*y, "
+                              "LN(r)*(1+scale)+shift")
     if "qk" in which:
         w = synth.qk_glm()
         rows = 4360 * 32
@@ -598,7 +609,8 @@ def run_ours(args):
                               "k's op and step k-1's output; CUDA events around all steps",
                        "one_stream_ms_per_step": round(serial_ms, 4)}
     if rank == 0 and not args.no_per_config:
-        names = ["tiny", "sana", "sana_nmod2", "glm_ln", "glm_gate", "qk", "gelu_bf16", "gelu_fp16"]
+        names = ["tiny", "sana", "sana_nmod2", "glm_ln", "glm_gate", "glm_gate_ln", "qk", "gelu_bf16",
+                 "gelu_fp16"]
         per = {}
         steps = max(20, min(args.steps, 400))
         for name in names:
@@ -642,8 +654,8 @@ def main():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--quick", action="store_true", help="headline only (for profiler runs)")
     p.add_argument("--only", default="sana",
-                   choices=["sana", "sana_nmod2", "tiny", "glm_ln", "glm_gate", "qk", "gelu_bf16",
-                            "gelu_fp16"],
+                   choices=["sana", "sana_nmod2", "tiny", "glm_ln", "glm_gate", "glm_gate_ln", "qk",
+                            "gelu_bf16", "gelu_fp16"],
                    help="workload timed as the headline (profiling runs); the JSON line's metric "
                         "and roofline describe the Sana LN+modulate only when this is 'sana'")
     args = p.parse_args()

@@ -205,6 +205,47 @@ adaln_status adaln_can_residual_gate_add(const void *out, const void *x, const v
                                          int dtype, uint32_t flags);
 
 /* ------------------------------------------------------------------------
+ * adaln_residual_gate_ln_modulate
+ *   r_out[b, n, :] = x[b, n, :] + gate[b, :] * y[b, n, :]
+ *   out[b, n, :]   = LN(r_out[b, n, :]) * (1 + scale[b, :]) + shift[b, :]
+ *
+ * The "scale_residual_norm_scale_shift" of the Fused Kernels page (Kernel
+ * inventory, Normalization table: the norm + scale/shift chain together
+ * with the preceding residual + gate * update), with the LayerNorm of
+ * adaln_ln_modulate: the residual gate-add and the following LN+modulate of
+ * a DiT block in one pass, x and y read once, r and out written once.
+ *   x, y, r_out, out contiguous (B, N, D); gate, scale, shift rows at
+ *   ptr + b * stride, contiguous over D (stride 0 broadcasts one row).
+ *   r_out may equal x or y (an in-place residual update); out overlaps none
+ *   of the others.
+ *   Limits: those of adaln_residual_gate_add and adaln_ln_modulate (D % 4
+ *   == 0, eps finite and >= 0).  One kernel when D <= 4096, the rows are
+ *   8-byte aligned and the gate rows are 8-byte aligned with s_gate_b % 4
+ *   == 0; otherwise the gate-add kernel writes r_out and the LN+modulate
+ *   kernel reads it back (two launches on the stream, same bits).
+ * Numerics: r_out = round(x + round(gate * y)); out is adaln_ln_modulate of
+ * r_out as stored (bit for bit the two calls in sequence).
+ * Returns the statuses of the two calls it combines; ADALN_E_OVERLAP also
+ * when out overlaps x, y, r_out or the gate rows, or r_out overlaps the
+ * scale or shift rows.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_residual_gate_ln_modulate(void *r_out, void *out, const void *x,
+                                             const void *gate, int64_t s_gate_b,
+                                             const void *y, int64_t B, int64_t N, int64_t D,
+                                             const void *scale, int64_t s_scale_b,
+                                             const void *shift, int64_t s_shift_b,
+                                             float eps, int dtype, uint32_t flags,
+                                             void *stream);
+
+adaln_status adaln_can_residual_gate_ln_modulate(const void *r_out, const void *out,
+                                                 const void *x, const void *gate,
+                                                 int64_t s_gate_b, const void *y,
+                                                 int64_t B, int64_t N, int64_t D,
+                                                 const void *scale, int64_t s_scale_b,
+                                                 const void *shift, int64_t s_shift_b,
+                                                 float eps, int dtype, uint32_t flags);
+
+/* ------------------------------------------------------------------------
  * adaln_bias_gelu_tanh
  *   out[r, c] = gelu_tanh(round(x[r, c] + bias[c]))
  *

@@ -258,6 +258,29 @@ def residual_gate_add(x: np.ndarray, gate_base: np.ndarray, gate_offset: int, s_
     return idx, out
 
 
+def residual_gate_ln_modulate(x: np.ndarray, gate_base: np.ndarray, gate_offset: int, s_gate_b: int,
+                              y: np.ndarray, B: int, N: int, D: int, scale_base: np.ndarray,
+                              scale_offset: int, s_scale_b: int, shift_base: np.ndarray,
+                              shift_offset: int, s_shift_b: int, eps: float, dtype: str = "bf16",
+                              rows: Optional[Sequence[int]] = None, threads: int = 1):
+    """``r = x + gate*y``, then ``LN(r)*(1+scale)+shift`` of r as stored: the
+    Fused Kernels page's scale_residual_norm_scale_shift (Kernel inventory,
+    Normalization table) is exactly the gate-add chain followed by the
+    LN+modulate chain, so this is their composition.  Returns (row_ids, r, out)."""
+    ids, r = residual_gate_add(x, gate_base, gate_offset, s_gate_b, y, B, N, D, dtype, rows=rows,
+                               threads=threads)
+    out = np.empty_like(r)
+    # LN+modulate row by row of r (rows of one sample share the scale / shift row)
+    for b in np.unique(ids // N):
+        sel = np.nonzero(ids // N == b)[0]
+        rb = np.ascontiguousarray(r[sel])
+        _, ob = ln_modulate(rb, 1, sel.size, D, (sel.size * D, D, 1), scale_base,
+                            scale_offset + int(b) * s_scale_b, 0, shift_base,
+                            shift_offset + int(b) * s_shift_b, 0, eps, dtype, threads=threads)
+        out[sel] = ob
+    return ids, r, out
+
+
 def bias_gelu_tanh(x: np.ndarray, bias: np.ndarray, rows_total: int, width: int,
                    dtype: str = "bf16", rows: Optional[Sequence[int]] = None,
                    threads: int = 1):

@@ -117,3 +117,24 @@ def test_gate_and_gelu_validation(ad):
     assert b(OUT, X, None, 10, 10, 0, 0) == 1
     assert b(OUT, X, OUT + 4, 10, 10, 0, 0) == 7
     assert b(OUT, X, SC, 10, 10, 3, 0) == 2
+
+
+def test_residual_ln_validation(ad):
+    f = ad.capi.adaln_can_residual_gate_ln_modulate
+    R, O, Y = 1 << 36, 1 << 37, 1 << 38       # x, y, r, out far apart (33.5 MB each)
+    G, S, H = 1 << 39, (1 << 39) + 16384, (1 << 39) + 32768
+    args = lambda r=R, o=O, x=X, g=G, y=Y, D=4096, eps=1e-5, dt=0, fl=0: (
+        r, o, x, g, 0, y, 1, 4096, D, S, 0, H, 0, eps, dt, fl)
+    assert f(*args()) == 0
+    assert f(*args(r=X)) == 0                   # in-place residual update on x
+    assert f(*args(r=Y)) == 0                   # or on y
+    assert f(*args(o=R)) == 7                   # out on r
+    assert f(*args(o=X)) == 7                   # out on x
+    assert f(*args(o=Y + 64)) == 7              # out into y
+    assert f(*args(r=S - 8)) == 7               # r into the scale row
+    assert f(*args(D=4098)) == 3                # D % 4 != 0
+    assert f(*args(eps=-1.0)) == 6
+    assert f(*args(dt=2)) == 2
+    assert f(*args(fl=4)) == 6
+    assert f(*args(g=0)) == 1
+    assert f(*args(x=X + 1)) == 4               # odd address

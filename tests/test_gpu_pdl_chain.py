@@ -1,4 +1,4 @@
-"""All four ops chained on one stream with programmatic dependent launch:
+"""All ops chained on one stream with programmatic dependent launch:
 each op reads what the op before it wrote, so a kernel that read its input
 before its producer finished would return wrong bits.  Every kernel lets its
 dependents launch right after its own wait; the chain runs eagerly and as a
@@ -41,7 +41,8 @@ def chain_ref():
     # 2048 tokens of 512 channels (the TMA tile kernel)
     lt = oracle.ln_modulate(r, 1, D, N, (N * D, 1, D), gsc, N, 0, gsc, 2 * N, 0, 1e-6,
                             threads=THREADS)[1]
-    return dict(x=x, bias=bias, y=y, gsc=gsc, wq=wq, bq=bq, g=g, r=r, ln=ln, qk=qk, lt=lt)
+    # the fused residual gate-add + LN+modulate of g gives r and ln again
+    return dict(x=x, bias=bias, y=y, gsc=gsc, wq=wq, bq=bq, g=g, r=r, ln=ln, qk=qk, lt=lt, rf=r, lf=ln)
 
 
 def _chain(ad, t):
@@ -54,6 +55,8 @@ def _chain(ad, t):
                    flags=pdl)
     ad.qk_head_layernorm(t["ln"].view(-1, DH), None, t["wq"], t["bq"], t["wq"], t["bq"], 1e-6,
                          q_out=t["qk"].view(-1, DH), flags=pdl)
+    ad.residual_gate_ln_modulate(t["g"].view(B, N, D), rows[0], t["y"].view(B, N, D), rows[1], rows[2], 1e-6,
+                                 r_out=t["rf"].view(B, N, D), out=t["lf"].view(B, N, D), flags=pdl)
     flat = t["gsc"].view(-1)
     ad.ln_modulate(t["r"].view(1, N, D).permute(0, 2, 1), flat[N:2 * N].view(1, N),
                    flat[2 * N:3 * N].view(1, N), 1e-6, out=t["lt"].view(1, D, N), flags=pdl)
@@ -61,14 +64,14 @@ def _chain(ad, t):
 
 def _tensors(ref):
     t = {k: dev_tensor(ref[k]) for k in ("x", "bias", "y", "gsc", "wq", "bq")}
-    for k in ("g", "r", "ln", "qk", "lt"):
+    for k in ("g", "r", "ln", "qk", "lt", "rf", "lf"):
         t[k] = torch.zeros((N, D), dtype=torch.bfloat16, device="cuda")
     return t
 
 
 def _check(t, ref, what):
     torch.cuda.synchronize()
-    for k in ("g", "r", "ln", "qk", "lt"):
+    for k in ("g", "r", "ln", "qk", "lt", "rf", "lf"):
         assert_bits_equal(host_bits(t[k]).reshape(-1), ref[k].reshape(-1), what=f"{what}: {k}")
 
 
@@ -77,7 +80,7 @@ def test_chain_eager(ad, chain_ref):
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         for _ in range(3):
-            for k in ("g", "r", "ln", "qk", "lt"):
+            for k in ("g", "r", "ln", "qk", "lt", "rf", "lf"):
                 t[k].zero_()          # a plain kernel between the chains
             _chain(ad, t)
     s.synchronize()
@@ -93,7 +96,7 @@ def test_chain_in_a_graph(ad, chain_ref):
         s.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            for k in ("g", "r", "ln", "qk", "lt"):
+            for k in ("g", "r", "ln", "qk", "lt", "rf", "lf"):
                 t[k].zero_()
             _chain(ad, t)
     for _ in range(3):
