@@ -32,7 +32,7 @@ constexpr int kOpshMaxBytes = 32 * 1024;
 // gate-add chain, x and y contiguous), written to r_out, and the LayerNorm
 // and modulate run on r: one read of x and y, one write of r and out.
 // With OPSH the gate rows join the shared table (after the op / shift
-// pairs, B * D * 2 more bytes).
+// pairs, B * D * 2 more bytes; the whole table stays within kOpshMaxBytes).
 struct RowsGate {
     const uint16_t *y;
     const uint16_t *gate;
@@ -249,11 +249,14 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
     }
 }
 
+static inline int64_t rows_opsh_bytes(const LnArgs &a, bool gate) { return a.B * a.D * (gate ? 6 : 4); }
+
 template <DT T, int NI, bool TAIL, bool OPSH, bool GATE>
 static cudaError_t run_rows(const LnArgs &a, const RowsGate &g, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     auto k = ln_rows_kernel<T, NI, TAIL, OPSH, GATE>;
-    // <= 48 KiB (B D 4 <= 32 KiB when OPSH): no opt-in needed
-    const size_t smem = OPSH ? (size_t)(a.B * a.D * (GATE ? 6 : 4)) : 0;
+    // <= kOpshMaxBytes with OPSH (rows_opsh_ok), which leaves room for the
+    // static shared memory under the 48 KiB a launch gets without opt-in
+    const size_t smem = OPSH ? (size_t)rows_opsh_bytes(a, GATE) : 0;
     const int64_t rows = a.B * a.N;
     const int64_t ctas_needed = (rows + kRowsThreads / 32 - 1) / (kRowsThreads / 32);
     const int64_t grid = imin64(ctas_needed, (int64_t)dev.sms * blocks_per_sm(k, kRowsThreads, smem));
@@ -263,14 +266,15 @@ static cudaError_t run_rows(const LnArgs &a, const RowsGate &g, bool pdl, cudaSt
                     a.eps, g);
 }
 
-// the op / shift table of all samples fits in shared memory (the rows path
-// already guarantees 8-byte aligned scale / shift and even strides)
-static inline bool rows_opsh_ok(const LnArgs &a) { return a.B * a.D * 4 <= kOpshMaxBytes; }
+// the op / shift table of all samples (and with GATE the gate rows) fits in
+// shared memory (the rows path already guarantees 8-byte aligned scale /
+// shift and even strides)
+static inline bool rows_opsh_ok(const LnArgs &a, bool gate) { return rows_opsh_bytes(a, gate) <= kOpshMaxBytes; }
 
 template <DT T, int NI, bool GATE>
 static cudaError_t rows_tail(const LnArgs &a, const RowsGate &g, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     const bool tail = a.D % 512 != 0;
-    if (rows_opsh_ok(a))
+    if (rows_opsh_ok(a, GATE))
         return tail ? run_rows<T, NI, true, true, GATE>(a, g, pdl, s, dev)
                     : run_rows<T, NI, false, true, GATE>(a, g, pdl, s, dev);
     return tail ? run_rows<T, NI, true, false, GATE>(a, g, pdl, s, dev)

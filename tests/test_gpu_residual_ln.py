@@ -58,8 +58,15 @@ def test_broadcast_rows_and_in_place(ad):
 
 
 def test_large_batch_without_the_shared_table(ad):
-    # B * D * 4 > 32 KiB: gate / scale / shift read from global memory
+    # B * D * 6 > 32 KiB: gate / scale / shift read from global memory
     case(ad, 9, 24, 1024, seed=6)
+
+
+@pytest.mark.parametrize("B,D", [(2, 2728), (2, 2732), (2, 4096), (4, 1364), (4, 2048)])
+def test_shared_table_size_edge(ad, B, D):
+    # the gate, op and shift table takes B * D * 6 bytes: 32736 (the last
+    # size kept in shared memory), then 32784, 49152, 32736, 49152
+    case(ad, B, 17, D, seed=B * D)
 
 
 def test_matches_the_two_ops_in_sequence(ad):
