@@ -255,6 +255,47 @@ def make_workloads(dev, which, n_sets=None, flags=0):
     return out
 
 
+def make_eager(dev, name, nb):
+    """The same workload as torch eager ops on rotating sets (context only):
+    the chain each fused op replaces, as a model would run it; nb is the
+    fused op's algorithmic bytes, which sizes the rotation."""
+    import torch
+    import torch.nn.functional as F
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sets = max(1, min(MAX_SETS, -(-4 * l2 // nb)))
+    g = lambda shape, std=1.0: (std * torch.randn(shape, device=dev)).to(torch.bfloat16)
+    out = []
+    for _ in range(sets):
+        if name in ("sana", "sana_nmod2"):
+            nm = 6 if name == "sana" else 2
+            xb, tb = g((2, 2240, 1024)), g((2, nm, 2240), 0.1)
+            out.append(lambda xb=xb, tb=tb: F.layer_norm(xb.permute(0, 2, 1), (2240,), eps=1e-6)
+                       * (1 + tb[:, 1:2]) + tb[:, 0:1])
+        elif name in ("tiny", "glm_ln"):
+            shape = (1, 64, 512) if name == "tiny" else (1, 4096, 4096)
+            x, sc, sh = g(shape), g((1, 1, shape[2]), 0.1), g((1, 1, shape[2]), 0.1)
+            out.append(lambda x=x, sc=sc, sh=sh, D=shape[2]: F.layer_norm(x, (D,), eps=1e-5) * (1 + sc) + sh)
+        elif name == "glm_gate":
+            x, y, gt = g((1, 4096, 4096)), g((1, 4096, 4096)), g((1, 1, 4096), 0.1)
+            out.append(lambda x=x, y=y, gt=gt: x + gt * y)
+        elif name == "glm_gate_ln":
+            x, y, gt, sc, sh = g((1, 4096, 4096)), g((1, 4096, 4096)), g((1, 1, 4096), 0.1), g((1, 1, 4096), 0.1), \
+                g((1, 1, 4096), 0.1)
+            out.append(lambda x=x, y=y, gt=gt, sc=sc, sh=sh: (
+                lambda r: (r, F.layer_norm(r, (4096,), eps=1e-5) * (1 + sc) + sh))(x + gt * y))
+        elif name == "qk":
+            q, k = g((1, 4360, 32, 128), 2.0), g((1, 4360, 32, 128), 2.0)
+            w = [g((128,), 0.05) for _ in range(4)]
+            out.append(lambda q=q, k=k, w=w: (F.layer_norm(q, (128,), w[0], w[1], 1e-6),
+                                              F.layer_norm(k, (128,), w[2], w[3], 1e-6)))
+        elif name.startswith("gelu_"):
+            dt = torch.bfloat16 if name == "gelu_bf16" else torch.float16
+            x, b = g((32760, 13824)).to(dt), g((13824,), 0.02).to(dt)
+            out.append(lambda x=x, b=b: F.gelu(x + b, approximate="tanh"))
+    return out
+
+
 # ------------------------------------------------------------ timing
 
 class Flusher:
@@ -620,6 +661,10 @@ def run_ours(args):
             iso = time_calls(cl[0], max(10, min(args.steps, 200)), 5, flush)
             cc = copy_calls(dev, nb)
             msc = time_block(cc, steps, 3)
+            del cc
+            ec = make_eager(dev, name, nb)
+            mse = time_block(ec, min(steps, 100), 3)
+            del ec
             us, usc = ms * 1e3, msc * 1e3
             per[name] = {"workload": desc, "us_per_call": round(us, 3),
                          "gbs": round(nb / (us * 1e-6) / 1e9, 1),
@@ -628,12 +673,14 @@ def run_ours(args):
                          "rotating_mib": round(len(cl) * nb / 2**20, 1),
                          "isolated_call_us_median": round(statistics.median(iso) * 1e3, 3),
                          "copy_same_bytes_us": round(usc, 3),
-                         "copy_same_bytes_gbs": round(nb / (usc * 1e-6) / 1e9, 1)}
-            del wl, cl, cc
+                         "copy_same_bytes_gbs": round(nb / (usc * 1e-6) / 1e9, 1),
+                         "torch_eager_us": round(mse * 1e3, 3)}
+            del wl, cl
             torch.cuda.empty_cache()
         line["per_config"] = per
         line["per_config_how"] = ("each workload timed like the headline (rotating sets >= 4x L2, CUDA "
-                                  "graphs, PDL) next to a same-byte SM copy timed the same way")
+                                  "graphs, PDL) next to a same-byte SM copy and the torch eager chain the "
+                                  "op replaces (context only), timed the same way")
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
