@@ -15,6 +15,11 @@ Parity status of each function (what pins it, see ``tests/test_oracle_*``):
                      cases, modulate identities, bit-level symmetries
   qk_head_layernorm  pinned: fp64 two-pass LayerNorm with affine, exact cases
   residual_gate_add  pinned: single-rounding fp64 definition
+  norm_scale_shift   pinned: LN mode equals ln_modulate / the gate-add + LN
+                     composition; RMS mode: fp64 RMSNorm, exact rows,
+                     sign-flip and power-of-two symmetries; per-token rows
+                     and gates equal per-row calls of the pinned forms
+  qk_rmsnorm         pinned: fp64 RMSNorm with weight, exact rows
   bias_gelu_tanh     pinned: 100-bit evaluation of tanh-GELU on all inputs
   rsqrt_cr           pinned: 100-bit evaluation
 """
@@ -72,6 +77,10 @@ def _lib_handle():
                 "oracle_bias_gelu_tanh": [_P, _P, _P, _I, _I, _INT, _I, _I],
                 "oracle_gelu_table": [_P, _INT],
                 "oracle_row_stats": [_P, _I, _INT, _P, _P],
+                "oracle_row_sumsq": [_P, _I, _INT, _P],
+                "oracle_norm_scale_shift": [_P, _P, _INT, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _I, _P,
+                                            _P, _I, _I, _P, _I, _I, _F, _INT, _I, _I, _P, _P],
+                "oracle_qk_rmsnorm": [_P, _P, _I, _I, _P, _F, _INT, _I, _I],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -281,6 +290,90 @@ def residual_gate_ln_modulate(x: np.ndarray, gate_base: np.ndarray, gate_offset:
     return ids, r, out
 
 
+NORM_CODE = {"layer": 0, "rms": 1}
+
+
+def norm_scale_shift(norm: str, x_base: np.ndarray, B: int, N: int, D: int,
+                     strides: Tuple[int, int, int], scale_base: np.ndarray, scale_offset: int,
+                     s_scale_b: int, s_scale_n: int, shift_base: np.ndarray, shift_offset: int,
+                     s_shift_b: int, s_shift_n: int, eps: float, dtype: str = "bf16",
+                     gate: Optional[Tuple[np.ndarray, int, int, int, int]] = None,
+                     y: Optional[np.ndarray] = None, rows: Optional[Sequence[int]] = None,
+                     threads: int = 1, return_stats: bool = False):
+    """LayerNorm (``norm="layer"``) or RMSNorm (``"rms"``), no affine, then
+    ``* (1 + scale) + shift``, optionally after the residual gate-add
+    ``r = x + gate * y`` (Fused Kernels page, Normalization table:
+    rmsnorm_scale_shift, scale_residual_norm_scale_shift; request-gated
+    fusion table: per-token [B, S, 1] gates, strided [B, S, 6D] chunk views).
+
+    Element (b, n, d) of x sits at ``b*sxB + n*sxN + d*sxD`` of ``x_base``;
+    of scale at ``scale_offset + b*s_scale_b + n*s_scale_n + d`` (shift
+    likewise).  ``gate = (base, offset, s_b, s_n, s_d)`` places gate
+    (b, n, d) at ``offset + b*s_b + n*s_n + d*s_d`` (s_d = 0 for a per-token
+    scalar); y is contiguous (B, N, D).  Returns ``(row_ids, out)``, or
+    ``(row_ids, r, out)`` with a gate; with ``return_stats`` also the per-row
+    binary32 mean (0 for RMSNorm) and rstd."""
+    lib = _lib_handle()
+    xb, sb, hb = _u16(x_base).reshape(-1), _u16(scale_base).reshape(-1), _u16(shift_base).reshape(-1)
+    idx, runs = _segments(rows, B * N)
+    out = np.zeros((idx.size, D), dtype=np.uint16)
+    r_out = np.zeros((idx.size, D), dtype=np.uint16) if gate is not None else None
+    mean = np.zeros(idx.size, dtype=np.float32)
+    rstd = np.zeros(idx.size, dtype=np.float32)
+    pos = {int(r): i for i, r in enumerate(idx)}
+    sxB, sxN, sxD = strides
+    if gate is not None:
+        gb, goff, sgb, sgn, sgd = gate
+        gb = _u16(gb).reshape(-1)
+        yb = _u16(y).reshape(-1)
+        if yb.size < B * N * D:
+            raise ValueError("y must hold B*N*D values")
+
+    def one(piece):
+        b0, e0 = piece
+        i0 = pos[b0]
+        if gate is not None:
+            gargs = (gb.ctypes.data + 2 * goff, sgb, sgn, sgd, yb.ctypes.data)
+            rptr = r_out[i0:].ctypes.data
+        else:
+            gargs, rptr = (None, 0, 0, 0, None), None
+        rc = lib.oracle_norm_scale_shift(rptr, out[i0:].ctypes.data, NORM_CODE[norm], xb.ctypes.data,
+                                         B, N, D, sxB, sxN, sxD, *gargs,
+                                         sb.ctypes.data + 2 * scale_offset, s_scale_b, s_scale_n,
+                                         hb.ctypes.data + 2 * shift_offset, s_shift_b, s_shift_n, eps,
+                                         DTYPE_CODE[dtype], b0, e0, mean[i0:].ctypes.data,
+                                         rstd[i0:].ctypes.data)
+        if rc:
+            raise ValueError(f"oracle_norm_scale_shift rejected its arguments ({rc})")
+
+    _run(_split_runs(runs, threads), one, threads)
+    res = (idx, out) if gate is None else (idx, r_out, out)
+    return res + (mean, rstd) if return_stats else res
+
+
+def qk_rmsnorm(x: np.ndarray, Dh: int, w: np.ndarray, eps: float, dtype: str = "bf16",
+               rows: Optional[Sequence[int]] = None, threads: int = 1):
+    """Per-head RMSNorm with a weight on a (rows, Dh) tensor (Fused Kernels
+    page, Normalization table: qk_rmsnorm_native); returns (row_ids, out)."""
+    lib = _lib_handle()
+    xf = _u16(x).reshape(-1)
+    nrows = xf.size // Dh
+    w = _u16(w).reshape(-1)
+    idx, runs = _segments(rows, nrows)
+    out = np.zeros((idx.size, Dh), dtype=np.uint16)
+    pos = {int(r): i for i, r in enumerate(idx)}
+
+    def one(piece):
+        b0, e0 = piece
+        rc = lib.oracle_qk_rmsnorm(out[pos[b0]:].ctypes.data, xf.ctypes.data, nrows, Dh, w.ctypes.data,
+                                   eps, DTYPE_CODE[dtype], b0, e0)
+        if rc:
+            raise ValueError(f"oracle_qk_rmsnorm rejected its arguments ({rc})")
+
+    _run(_split_runs(runs, threads), one, threads)
+    return idx, out
+
+
 def bias_gelu_tanh(x: np.ndarray, bias: np.ndarray, rows_total: int, width: int,
                    dtype: str = "bf16", rows: Optional[Sequence[int]] = None,
                    threads: int = 1):
@@ -340,6 +433,15 @@ def rsqrt_cr(x: np.ndarray) -> np.ndarray:
     out = np.empty_like(x)
     _lib_handle().oracle_rsqrt_cr_array(x.ctypes.data, out.ctypes.data, x.size)
     return out
+
+
+def row_sumsq(row: np.ndarray, lanes: int = 128) -> float:
+    """RMSNorm sum of squares of one binary32 row on the canonical lane DAG."""
+    row = np.ascontiguousarray(row, dtype=np.float32)
+    ss = np.zeros(1, dtype=np.float32)
+    if _lib_handle().oracle_row_sumsq(row.ctypes.data, row.size, lanes, ss.ctypes.data):
+        raise ValueError("bad row length / lane count")
+    return float(ss[0])
 
 
 def row_stats(row: np.ndarray, lanes: int = 128) -> Tuple[float, float]:

@@ -22,6 +22,12 @@
  *  - qk_head_layernorm: "Fused Kernels", Normalization table; PR #34008
  *    "实现拆解" 1 (per-head LayerNorm on q and k in one kernel).
  *  - residual_gate_add: "Fused Kernels", adaLN modulation and gating table.
+ *  - rmsnorm_scale_shift, scale_residual_norm_scale_shift, qk_rmsnorm_native:
+ *    "Fused Kernels", Normalization table (RMSNorm + `* (1 + scale) + shift`;
+ *    the same after `residual + gate * update`; per-head QK RMSNorm), the
+ *    request-gated fusion table (per-token [B, S, 1] gate, strided
+ *    [B, S, 6D] chunk views of the modulation rows) and "Numerical contracts
+ *    and quality tiers" (the RMSNorm statistics are folded by a butterfly).
  *  - bias_gelu_tanh: PR #37075 "功能与动机" and "关键源码片段" (fp32 add,
  *    round to the storage type, then tanh-GELU, round again).
  *
@@ -31,7 +37,12 @@
  * the correctly rounded 1/sqrt; var = m2 / D; the combine is Chan's pairwise
  * formula with a guarded coefficient; the fold is a butterfly over logical
  * lane bits in the order 16, 8, 4, 2, 1 then 64, 32; GELU's fp32 value is the
- * correctly rounded exact tanh-GELU.
+ * correctly rounded exact tanh-GELU.  RMSNorm: each lane sums x*x over its
+ * chunks with the square and the sum rounded separately (no fused
+ * multiply-add), the lanes are folded by the same butterfly with plain
+ * additions, ms = ss / D, rstd = rsqrt_cr(ms + eps), and the normalised value
+ * is round16(rstd * x), the LayerNorm's formula with mean 0.  The per-head
+ * QK RMSNorm scales by its weight in binary32 and rounds once to storage.
  */
 #include <math.h>
 #include <stdint.h>
@@ -183,6 +194,9 @@ static wstate chan_combine(wstate a, wstate b) {
  * butterfly: at each stage offset o every lane l becomes
  * combine(state[l & ~o], state[l | o]).  Offsets 16, 8, 4, 2, 1 (inside a
  * group of 32 lanes) and then, for L = 128, 64, 32 (across groups). */
+static const int order128[7] = {16, 8, 4, 2, 1, 64, 32};
+static const int order32[5] = {16, 8, 4, 2, 1};
+
 static void row_stats(const float *x, int64_t D, int L, float *mean, float *m2) {
     wstate st[128], nx[128];
     int64_t nvec = D / 4;
@@ -191,8 +205,6 @@ static void row_stats(const float *x, int64_t D, int L, float *mean, float *m2) 
         for (int64_t j = l; j < nvec; j += L)
             for (int e = 0; e < 4; ++e) welford_push(&st[l], x[4 * j + e]);
     }
-    static const int order128[7] = {16, 8, 4, 2, 1, 64, 32};
-    static const int order32[5] = {16, 8, 4, 2, 1};
     const int *order = (L == 128) ? order128 : order32;
     int stages = (L == 128) ? 7 : 5;
     for (int s = 0; s < stages; ++s) {
@@ -210,43 +222,104 @@ static float stats_rstd(float m2, int64_t D, float eps) {
     return oracle_rsqrt_cr(var + eps);
 }
 
+/* Sum of squares of one row on L logical lanes, for RMSNorm.  Lane l owns
+ * the same vec4 chunks as in row_stats and accumulates s = s + x*x over
+ * them in increasing chunk and element order (the square rounded to
+ * binary32, then the sum: two roundings); lanes past the tail add nothing.
+ * Then the butterfly of row_stats with s[l] = s[l & ~o] + s[l | o]. */
+static float row_sumsq(const float *x, int64_t D, int L) {
+    float st[128], nx[128];
+    int64_t nvec = D / 4;
+    for (int l = 0; l < L; ++l) {
+        st[l] = 0.0f;
+        for (int64_t j = l; j < nvec; j += L)
+            for (int e = 0; e < 4; ++e) {
+                float sq = x[4 * j + e] * x[4 * j + e];
+                st[l] = st[l] + sq;
+            }
+    }
+    const int *order = (L == 128) ? order128 : order32;
+    int stages = (L == 128) ? 7 : 5;
+    for (int s = 0; s < stages; ++s) {
+        int o = order[s];
+        for (int l = 0; l < L; ++l) nx[l] = st[l & ~o] + st[l | o];
+        memcpy(st, nx, sizeof(float) * (size_t)L);
+    }
+    return st[0];
+}
+
+/* ms = ss / D; rstd = rsqrt_cr(ms + eps) */
+static float rms_rstd(float ss, int64_t D, float eps) {
+    float ms = ss / (float)D;
+    return oracle_rsqrt_cr(ms + eps);
+}
+
+/* r = round16(x + round16(gate * y)): the residual gate-add of one element */
+static float gate_add(float xv, uint16_t g, uint16_t yv, int dtype) {
+    float gy = round16(load16(g, dtype) * load16(yv, dtype), dtype);
+    return round16(xv + gy, dtype);
+}
+
 /* ------------------------------------------------------------------ */
-/* ln_modulate                                                          */
+/* norm + adaLN modulate (LayerNorm or RMSNorm, optional residual gate)  */
 /* ------------------------------------------------------------------ */
 
 /*
- * out[b, n, :] = modulate(LN(x[b, n, :]))  for rows r = b*N + n in
- * [row_begin, row_end).  x element (b, n, d) is at x[b*sxB + n*sxN + d*sxD];
- * out is contiguous (B, N, D); scale / shift row b starts at
- * scale + b*s_scale_b (contiguous over d).  Per element:
- *   y   = round16(rstd * (x - mean))
+ * out[b, n, :] = modulate(norm(v[b, n, :])) for rows r = b*N + n in
+ * [row_begin, row_end), where
+ *   v = x                                   when gate is NULL,
+ *   v = round16(x + round16(gate * y))      otherwise (the residual
+ *                                           gate-add; r_out, if not NULL,
+ *                                           receives v),
+ * x element (b, n, d) at x[b*sxB + n*sxN + d*sxD], y contiguous (B, N, D),
+ * gate (b, n, d) at gate[b*s_gate_b + n*s_gate_n + d*s_gate_d] (a per-token
+ * [B, S, 1] gate has s_gate_d = 0), scale / shift (b, n, d) at
+ * scale[b*s_scale_b + n*s_scale_n + d] (per-sample rows: s_scale_n = 0;
+ * per-token rows, e.g. chunks of a [B, S, 6D] table: s_scale_n = 6D).
+ * norm 0 is LayerNorm without affine (row_stats, stats_rstd); norm 1 is
+ * RMSNorm without affine (row_sumsq, rms_rstd, mean 0).  Per element:
+ *   y   = round16(rstd * (v - mean))
  *   op  = round16(1 + scale)
  *   p   = round16(y * op)
  *   out = round16(p + shift)
- * out points at the output of row row_begin (row r goes to
- * out + (r - row_begin) * D).  Optional row_mean / row_rstd, indexed the
- * same way, receive the statistics.
- * Returns 0, or -1 for D not a positive multiple of 4.
+ * Row r goes to out + (r - row_begin) * D (and r_out likewise).  Optional
+ * row_mean / row_rstd, indexed the same way, receive the statistics.
+ * Returns 0, or -1 for D not a positive multiple of 4 or a bad norm.
  */
-int oracle_ln_modulate(uint16_t *out, const uint16_t *x, int64_t B, int64_t N, int64_t D,
-                       int64_t sxB, int64_t sxN, int64_t sxD,
-                       const uint16_t *scale, int64_t s_scale_b,
-                       const uint16_t *shift, int64_t s_shift_b,
-                       float eps, int dtype, int64_t row_begin, int64_t row_end,
-                       float *row_mean, float *row_rstd) {
-    if (D <= 0 || D % 4) return -1;
+int oracle_norm_scale_shift(uint16_t *r_out, uint16_t *out, int norm,
+                            const uint16_t *x, int64_t B, int64_t N, int64_t D,
+                            int64_t sxB, int64_t sxN, int64_t sxD,
+                            const uint16_t *gate, int64_t s_gate_b, int64_t s_gate_n,
+                            int64_t s_gate_d, const uint16_t *y,
+                            const uint16_t *scale, int64_t s_scale_b, int64_t s_scale_n,
+                            const uint16_t *shift, int64_t s_shift_b, int64_t s_shift_n,
+                            float eps, int dtype, int64_t row_begin, int64_t row_end,
+                            float *row_mean, float *row_rstd) {
+    if (D <= 0 || D % 4 || (norm != 0 && norm != 1)) return -1;
     float *v = (float *)malloc(sizeof(float) * (size_t)D);
     if (!v) return -2;
     for (int64_t r = row_begin; r < row_end && r < B * N; ++r) {
         int64_t b = r / N, n = r % N;
         const uint16_t *xr = x + b * sxB + n * sxN;
         for (int64_t d = 0; d < D; ++d) v[d] = load16(xr[d * sxD], dtype);
-        float mean, m2;
-        row_stats(v, D, 128, &mean, &m2);
-        float rstd = stats_rstd(m2, D, eps);
+        if (gate) {
+            const uint16_t *g = gate + b * s_gate_b + n * s_gate_n;
+            for (int64_t d = 0; d < D; ++d) v[d] = gate_add(v[d], g[d * s_gate_d], y[r * D + d], dtype);
+            if (r_out)
+                for (int64_t d = 0; d < D; ++d) r_out[(r - row_begin) * D + d] = store16(v[d], dtype);
+        }
+        float mean, rstd;
+        if (norm == 0) {
+            float m2;
+            row_stats(v, D, 128, &mean, &m2);
+            rstd = stats_rstd(m2, D, eps);
+        } else {
+            mean = 0.0f;
+            rstd = rms_rstd(row_sumsq(v, D, 128), D, eps);
+        }
         if (row_mean) row_mean[r - row_begin] = mean;
         if (row_rstd) row_rstd[r - row_begin] = rstd;
-        const uint16_t *sc = scale + b * s_scale_b, *sh = shift + b * s_shift_b;
+        const uint16_t *sc = scale + b * s_scale_b + n * s_scale_n, *sh = shift + b * s_shift_b + n * s_shift_n;
         uint16_t *o = out + (r - row_begin) * D;
         for (int64_t d = 0; d < D; ++d) {
             float centered = v[d] - mean;
@@ -258,6 +331,20 @@ int oracle_ln_modulate(uint16_t *out, const uint16_t *x, int64_t B, int64_t N, i
     }
     free(v);
     return 0;
+}
+
+/* ln_modulate: LayerNorm (no affine) + adaLN modulate with one scale /
+ * shift row per sample (row b at scale + b*s_scale_b); out contiguous
+ * (B, N, D).  The norm 0, gate-free case of oracle_norm_scale_shift. */
+int oracle_ln_modulate(uint16_t *out, const uint16_t *x, int64_t B, int64_t N, int64_t D,
+                       int64_t sxB, int64_t sxN, int64_t sxD,
+                       const uint16_t *scale, int64_t s_scale_b,
+                       const uint16_t *shift, int64_t s_shift_b,
+                       float eps, int dtype, int64_t row_begin, int64_t row_end,
+                       float *row_mean, float *row_rstd) {
+    return oracle_norm_scale_shift(NULL, out, 0, x, B, N, D, sxB, sxN, sxD, NULL, 0, 0, 0, NULL,
+                                   scale, s_scale_b, 0, shift, s_shift_b, 0, eps, dtype,
+                                   row_begin, row_end, row_mean, row_rstd);
 }
 
 /* ------------------------------------------------------------------ */
@@ -288,6 +375,28 @@ int oracle_qk_head_layernorm(uint16_t *out, const uint16_t *in, int64_t rows, in
     return 0;
 }
 
+/* One tensor: rows of Dh contiguous values, RMSNorm with a weight on 32
+ * logical lanes: rstd = rsqrt_cr(ss / Dh + eps) with ss from row_sumsq,
+ * u = rstd * x, out = round16(w * u) (binary32 products, one storage
+ * rounding).  Rows [row_begin, row_end); row r goes to
+ * out + (r - row_begin) * Dh.  Returns -1 unless 0 < Dh <= 128 and
+ * Dh % 4 == 0. */
+int oracle_qk_rmsnorm(uint16_t *out, const uint16_t *in, int64_t rows, int64_t Dh,
+                      const uint16_t *w, float eps, int dtype, int64_t row_begin, int64_t row_end) {
+    if (Dh <= 0 || Dh > 128 || Dh % 4) return -1;
+    float v[128];
+    for (int64_t r = row_begin; r < row_end && r < rows; ++r) {
+        const uint16_t *xr = in + r * Dh;
+        for (int64_t d = 0; d < Dh; ++d) v[d] = load16(xr[d], dtype);
+        float rstd = rms_rstd(row_sumsq(v, Dh, 32), Dh, eps);
+        for (int64_t d = 0; d < Dh; ++d) {
+            float u = rstd * v[d];
+            out[(r - row_begin) * Dh + d] = store16(load16(w[d], dtype) * u, dtype);
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* residual_gate_add                                                    */
 /* ------------------------------------------------------------------ */
@@ -300,10 +409,8 @@ int oracle_residual_gate_add(uint16_t *out, const uint16_t *x, const uint16_t *g
                              int64_t D, int dtype, int64_t row_begin, int64_t row_end) {
     for (int64_t r = row_begin; r < row_end && r < B * N; ++r) {
         const uint16_t *g = gate + (r / N) * s_gate_b;
-        for (int64_t d = 0; d < D; ++d) {
-            float gy = round16(load16(g[d], dtype) * load16(y[r * D + d], dtype), dtype);
-            out[(r - row_begin) * D + d] = store16(load16(x[r * D + d], dtype) + gy, dtype);
-        }
+        for (int64_t d = 0; d < D; ++d)
+            out[(r - row_begin) * D + d] = store16(gate_add(load16(x[r * D + d], dtype), g[d], y[r * D + d], dtype), dtype);
     }
     return 0;
 }
@@ -384,6 +491,12 @@ void oracle_16_to_f32(const uint16_t *in, float *out, int64_t n, int dtype) {
 }
 void oracle_rsqrt_cr_array(const float *in, float *out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_rsqrt_cr(in[i]);
+}
+/* RMSNorm sum of squares on L lanes (128 or 32) of one binary32 row */
+int oracle_row_sumsq(const float *x, int64_t D, int L, float *ss) {
+    if (D <= 0 || D % 4 || (L != 128 && L != 32) || (L == 32 && D > 128)) return -1;
+    *ss = row_sumsq(x, D, L);
+    return 0;
 }
 /* row statistics on L lanes (128 or 32) of one binary32 row */
 int oracle_row_stats(const float *x, int64_t D, int L, float *mean, float *m2) {

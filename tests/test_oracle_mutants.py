@@ -23,6 +23,7 @@ import pytest
 import oracle
 import test_oracle_ln as ln
 import test_oracle_qk_gate_gelu as qg
+import test_oracle_rms as rm
 import test_oracle_rsqrt as rs
 import test_oracle_conversions as cv
 
@@ -42,14 +43,28 @@ MUTANTS = {
     "one_plus_scale_not_rounded": ("float op = round16(1.0f + load16(sc[d], dtype), dtype);",
                                    "float op = 1.0f + load16(sc[d], dtype);"),
     "product_not_rounded": ("float p = round16(y * op, dtype);", "float p = y * op;"),
-    "shift_scale_swapped": ("const uint16_t *sc = scale + b * s_scale_b, *sh = shift + b * s_shift_b;",
-                            "const uint16_t *sh = scale + b * s_scale_b, *sc = shift + b * s_shift_b;"),
+    "shift_scale_swapped": ("const uint16_t *sc = scale + b * s_scale_b + n * s_scale_n, *sh = shift + b * s_shift_b + n * s_shift_n;",
+                            "const uint16_t *sh = scale + b * s_scale_b + n * s_scale_n, *sc = shift + b * s_shift_b + n * s_shift_n;"),
     "tail_lanes_push_zeros": ("for (int64_t j = l; j < nvec; j += L)\n            for (int e = 0; e < 4; ++e) welford_push(&st[l], x[4 * j + e]);",
                               "for (int64_t j = l; j < ((nvec + L - 1) / L) * L; j += L)\n            for (int e = 0; e < 4; ++e) welford_push(&st[l], j < nvec ? x[4 * j + e] : 0.0f);"),
     "qk_w_b_swapped": ("store16(fmaf(load16(w[d], dtype), u, load16(bias[d], dtype)), dtype);",
                        "store16(fmaf(load16(bias[d], dtype), u, load16(w[d], dtype)), dtype);"),
-    "gate_product_not_rounded": ("float gy = round16(load16(g[d], dtype) * load16(y[r * D + d], dtype), dtype);",
-                                 "float gy = load16(g[d], dtype) * load16(y[r * D + d], dtype);"),
+    "gate_product_not_rounded": ("float gy = round16(load16(g, dtype) * load16(yv, dtype), dtype);",
+                                 "float gy = load16(g, dtype) * load16(yv, dtype);"),
+    "rms_subtracts_mean": ("            mean = 0.0f;\n            rstd = rms_rstd(",
+                           "            { float m2_; row_stats(v, D, 128, &mean, &m2_); }\n            rstd = rms_rstd("),
+    "rms_divisor_d_minus_1": ("float ms = ss / (float)D;", "float ms = ss / (float)(D - 1);"),
+    "rms_eps_dropped": ("return oracle_rsqrt_cr(ms + eps);", "return oracle_rsqrt_cr(ms);"),
+    "rms_abs_not_square": ("float sq = x[4 * j + e] * x[4 * j + e];", "float sq = fabsf(x[4 * j + e]);"),
+    "rms_fold_drops_upper": ("nx[l] = st[l & ~o] + st[l | o];", "nx[l] = st[l & ~o];"),
+    "per_token_scale_row_index": ("scale + b * s_scale_b + n * s_scale_n,", "scale + b * s_scale_b + b * s_scale_n,"),
+    "per_token_gate_row_ignored": ("const uint16_t *g = gate + b * s_gate_b + n * s_gate_n;",
+                                   "const uint16_t *g = gate + b * s_gate_b;"),
+    "gate_elem_stride_ignored": ("gate_add(v[d], g[d * s_gate_d], y[r * D + d], dtype)",
+                                 "gate_add(v[d], g[d], y[r * D + d], dtype)"),
+    "gated_norm_reads_x": ("for (int64_t d = 0; d < D; ++d) v[d] = gate_add(",
+                           "for (int64_t d = 0; d < D && 0; ++d) v[d] = gate_add("),
+    "qk_rms_weight_dropped": ("store16(load16(w[d], dtype) * u, dtype);", "store16(u, dtype);"),
     "gelu_constant_typo": ("const long double k1 = 0.044715L;", "const long double k1 = 0.04715L;"),
     "gelu_sign": ("long double g = v / (1.0L + expl(-2.0L * z));", "long double g = v / (1.0L + expl(2.0L * z));"),
     "gelu_bias_dropped": ("uint16_t v = store16(load16(x[r * width + c], dtype) + load16(bias[c], dtype), dtype);",
@@ -63,8 +78,11 @@ ORDER_ONLY = {
                             "static const int order128[7] = {1, 2, 4, 8, 16, 32, 64};"),
     "combine_operands_transposed": ("nx[l] = chan_combine(st[l & ~o], st[l | o]);",
                                     "nx[l] = chan_combine(st[l | o], st[l & ~o]);"),
-    "blocked_lane_assignment": ("for (int64_t j = l; j < nvec; j += L)",
-                                "for (int64_t j = l * ((nvec + L - 1) / L); j < nvec && j < (l + 1) * ((nvec + L - 1) / L); ++j)"),
+    "blocked_lane_assignment": ("for (int64_t j = l; j < nvec; j += L)\n            for (int e = 0; e < 4; ++e) welford_push",
+                                "for (int64_t j = l * ((nvec + L - 1) / L); j < nvec && j < (l + 1) * ((nvec + L - 1) / L); ++j)\n            for (int e = 0; e < 4; ++e) welford_push"),
+    "rms_square_fused_into_sum": ("float sq = x[4 * j + e] * x[4 * j + e];\n                st[l] = st[l] + sq;",
+                                  "st[l] = fmaf(x[4 * j + e], x[4 * j + e], st[l]);"),
+    "qk_rms_on_128_lanes": ("rms_rstd(row_sumsq(v, Dh, 32), Dh, eps)", "rms_rstd(row_sumsq(v, Dh, 128), Dh, eps)"),
 }
 
 
@@ -93,6 +111,17 @@ def _pins():
     P.append(("gelu_sum", lambda: qg.test_bias_gelu_rounds_the_sum_once(None, "bf16")))
     P.append(("gelu_table", lambda: qg.test_gelu_table_matches_high_precision(None, "bf16")))
     P.append(("rsqrt", lambda: rs.test_rsqrt_matches_100bit_reference(None)))
+    for D in (12, 2240, 5120):
+        P.append((f"rms_fp64_{D}", lambda D=D: rm.test_rms_within_one_ulp_of_fp64(None, D, "bf16")))
+    P.append(("rms_exact", lambda: rm.test_exact_rows_give_half(None, 2240, "bf16", (3, 3, 3, 1, 1, 1, 1, 1), 0.0)))
+    P.append(("rms_exact_eps", lambda: rm.test_exact_rows_give_half(None, 512, "bf16", (3, 3, 3, 1, 1, 1, 0, 0), 0.25)))
+    P.append(("rms_signs", lambda: rm.test_sign_flips_flip_only_those_outputs(None, 516)))
+    P.append(("rms_tail_def", lambda: rm.test_modulate_tail_matches_definition(None, "bf16")))
+    for norm in ("layer", "rms"):
+        P.append((f"gated_{norm}", lambda norm=norm: rm.test_gated_mode_is_gate_add_then_norm(None, norm)))
+        P.append((f"per_token_{norm}", lambda norm=norm: rm.test_per_token_rows_and_gates_equal_one_row_calls(None, norm)))
+    P.append(("qk_rms", lambda: rm.test_qk_rms_within_rounding_bound(None, 128, "bf16")))
+    P.append(("qk_rms_exact", lambda: rm.test_qk_rms_exact_rows(None, 64)))
     P.append(("bf16_encode", lambda: cv.test_bf16_encode_vs_torch(None)))
     P.append(("fp16_encode", lambda: cv.test_fp16_encode_vs_numpy(None)))
     return P
