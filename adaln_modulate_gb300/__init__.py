@@ -9,8 +9,9 @@ Two layers:
   * ``capi``: the C functions under their C names (``capi.adaln_ln_modulate``
     and so on), taking raw integers (device pointers, sizes, a stream handle);
   * ``ln_modulate``, ``qk_head_layernorm``, ``residual_gate_add``,
-    ``bias_gelu_tanh``: the same calls taking torch tensors (PyTorch only
-    provides the device memory and the current stream).
+    ``bias_gelu_tanh``, ``residual_gate_ln_modulate``, ``norm_scale_shift``,
+    ``rmsnorm_scale_shift``, ``qk_rmsnorm``: the same calls taking torch
+    tensors (PyTorch only provides the device memory and the current stream).
 """
 from __future__ import annotations
 
@@ -32,6 +33,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 BF16, FP16 = 0, 1
 FLAG_PDL = 1
+NORM = {"layer": 0, "rms": 1}
 STATUS = {0: "ADALN_OK", 1: "ADALN_E_NULL", 2: "ADALN_E_DTYPE", 3: "ADALN_E_SHAPE",
           4: "ADALN_E_ALIGN", 5: "ADALN_E_STRIDE", 6: "ADALN_E_VALUE", 7: "ADALN_E_OVERLAP",
           8: "ADALN_E_CUDA"}
@@ -61,6 +63,16 @@ _SIGS = {
                                         _INT),
     "adaln_can_residual_gate_ln_modulate": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U],
                                             _INT),
+    "adaln_norm_scale_shift": ([_INT, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _I, _P, _P, _I, _I, _P, _I,
+                                _I, _F, _INT, _U, _P], _INT),
+    "adaln_can_norm_scale_shift": ([_INT, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _I, _P, _P, _I, _I, _P,
+                                    _I, _I, _F, _INT, _U], _INT),
+    "adaln_norm_scale_shift_variant": ([_INT, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _I, _P, _P, _I, _I,
+                                        _P, _I, _I, _F, _INT, _U], _INT),
+    "adaln_rmsnorm_scale_shift": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _P, _I, _I, _F, _INT, _U, _P], _INT),
+    "adaln_can_rmsnorm_scale_shift": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _P, _I, _I, _F, _INT, _U], _INT),
+    "adaln_qk_rmsnorm": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _F, _INT, _U, _P], _INT),
+    "adaln_can_qk_rmsnorm": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _F, _INT, _U], _INT),
 }
 
 
@@ -243,6 +255,110 @@ def residual_gate_ln_modulate(x, gate, y, scale, shift, eps: float, r_out=None, 
                                               _dtype_code(x), flags, _stream(stream))
     _check(st, "adaln_residual_gate_ln_modulate")
     return r_out, out
+
+
+def _operand(t, B: int, N: int, D: int, name: str, scalar_ok: bool = False):
+    """(pointer, s_b, s_n, s_d) of an operand broadcast to (B, N, D): (D,),
+    (B, D) / (1, D) rows per sample, or a 3-d (B|1, N|1, D) view (per-token
+    rows, e.g. a chunk of a (B, N, 6, D) table); with ``scalar_ok`` also
+    (B|1, N|1, 1), one value per token.  Broadcast dimensions get stride 0."""
+    if t.dim() == 1:
+        t = t.view(1, 1, -1)
+    elif t.dim() == 2:
+        t = t.unsqueeze(1)
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be (D,), (B, D) or (B|1, N|1, D)")
+    b, n, d = t.shape
+    if b not in (1, B) or n not in (1, N) or d not in ((1, D) if scalar_ok else (D,)):
+        raise ValueError(f"{name} of shape {tuple(t.shape)} does not broadcast to ({B}, {N}, {D})")
+    if d > 1 and t.stride(2) != 1:
+        raise ValueError(f"{name} must be contiguous over D")
+    return (t.data_ptr(), t.stride(0) if b > 1 else 0, t.stride(1) if n > 1 else 0,
+            1 if d > 1 else 0)
+
+
+def _norm_call(fn, norm, x, scale, shift, eps, gate, y, r_out, out, flags, stream, variant=False):
+    torch = _torch()
+    B, N, D = x.shape
+    sp, ssb, ssn, _ = _operand(scale, B, N, D, "scale")
+    hp, hsb, hsn, _ = _operand(shift, B, N, D, "shift")
+    if gate is not None:
+        if y is None or tuple(y.shape) != (B, N, D) or not y.is_contiguous() or not x.is_contiguous():
+            raise ValueError("with a gate, x and y must be contiguous (B, N, D)")
+        gp, gsb, gsn, gsd = _operand(gate, B, N, D, "gate", scalar_ok=True)
+        if r_out is None and not variant:
+            r_out = torch.empty_like(x)
+        yp = y.data_ptr()
+    else:
+        gp, gsb, gsn, gsd, yp = None, 0, 0, 1, None
+    if out is None and not variant:
+        out = torch.empty((B, N, D), dtype=x.dtype, device=x.device)
+    ptr = lambda t, dflt=None: t.data_ptr() if t is not None else dflt
+    args = [NORM[norm], ptr(r_out, 1 << 41 if gate is not None else None), ptr(out, 1 << 40), x.data_ptr(), B, N,
+            D, *x.stride(), gp, gsb, gsn, gsd, yp, sp, ssb, ssn, hp, hsb, hsn, float(eps), _dtype_code(x), flags]
+    if variant:
+        return fn(*args)
+    _check(fn(*args, _stream(stream)), "adaln_norm_scale_shift")
+    return (r_out, out) if gate is not None else out
+
+
+def norm_scale_shift(x, scale, shift, eps: float, norm: str = "layer", gate=None, y=None, r_out=None, out=None,
+                     flags: int = 0, stream=None):
+    """``norm(v) * (1 + scale) + shift`` with ``norm`` "layer" (LayerNorm) or
+    "rms" (RMSNorm), both without affine, and v = x, or, with ``gate``,
+    v = x + gate * y (stored in ``r_out``; pass ``r_out=x`` to update x in
+    place).  x is (B, N, D) of any strides (contiguous with a gate); scale /
+    shift are (D,), (B, D), (B, 1, D) rows per sample or (B, N, D) views per
+    token; gate is a per-sample row, a per-token row, or (B, N, 1) one value
+    per token.  Returns out, or (r, out) with a gate."""
+    return _norm_call(capi.adaln_norm_scale_shift, norm, x, scale, shift, eps, gate, y, r_out, out, flags, stream)
+
+
+def norm_scale_shift_variant(x, scale, shift, eps: float, norm: str = "layer", gate=None, y=None, r_out=None,
+                             out=None) -> str:
+    """Which kernel norm_scale_shift takes for these tensors (no CUDA work)."""
+    v = _norm_call(capi.adaln_norm_scale_shift_variant, norm, x, scale, shift, eps, gate, y, r_out, out, 0, None,
+                   variant=True)
+    if v < 0:
+        raise AdalnError(-v, "adaln_norm_scale_shift_variant")
+    return VARIANTS[v]
+
+
+def rmsnorm_scale_shift(x, scale, shift, eps: float, out=None, flags: int = 0, stream=None):
+    """``RMSNorm(x) * (1 + scale) + shift`` (no affine): norm_scale_shift
+    with ``norm="rms"`` and no gate, through adaln_rmsnorm_scale_shift."""
+    torch = _torch()
+    B, N, D = x.shape
+    sp, ssb, ssn, _ = _operand(scale, B, N, D, "scale")
+    hp, hsb, hsn, _ = _operand(shift, B, N, D, "shift")
+    if out is None:
+        out = torch.empty((B, N, D), dtype=x.dtype, device=x.device)
+    st = capi.adaln_rmsnorm_scale_shift(out.data_ptr(), x.data_ptr(), B, N, D, *x.stride(), sp, ssb, ssn, hp, hsb,
+                                        hsn, float(eps), _dtype_code(x), flags, _stream(stream))
+    _check(st, "adaln_rmsnorm_scale_shift")
+    return out
+
+
+def qk_rmsnorm(q, k, wq, wk, eps: float, q_out=None, k_out=None, flags: int = 0, stream=None):
+    """Per-head RMSNorm with a weight of q and k (any leading shape, last dim
+    Dh, contiguous) in one launch.  Pass ``q_out=q`` for in place."""
+    torch = _torch()
+    Dh = q.shape[-1] if q is not None else k.shape[-1]
+    rq = q.numel() // Dh if q is not None else 0
+    rk = k.numel() // Dh if k is not None else 0
+    for t in (q, k):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("q / k must be contiguous")
+    if q is not None and q_out is None:
+        q_out = torch.empty_like(q)
+    if k is not None and k_out is None:
+        k_out = torch.empty_like(k)
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    ref = q if q is not None else k
+    st = capi.adaln_qk_rmsnorm(ptr(q_out), ptr(q), rq, ptr(k_out), ptr(k), rk, Dh, ptr(wq), ptr(wk), float(eps),
+                               _dtype_code(ref), flags, _stream(stream))
+    _check(st, "adaln_qk_rmsnorm")
+    return q_out, k_out
 
 
 def bias_gelu_tanh(x, bias, out=None, flags: int = 0, stream=None):

@@ -183,6 +183,74 @@ adaln_status check_residual_ln(const void *r_out, const void *out, const void *x
     return ADALN_OK;
 }
 
+// bytes from p to one past the last element of a (B, N, D) operand with
+// strides (sb, sn, sd)
+int64_t extent(int64_t B, int64_t N, int64_t D, int64_t sb, int64_t sn, int64_t sd) {
+    return 2 * ((B - 1) * sb + (N - 1) * sn + (D - 1) * sd + 1);
+}
+
+// the general norm + modulate: norm 0 LayerNorm / 1 RMSNorm, optional
+// residual gate (gate != NULL), per-sample or per-token operand rows
+adaln_status check_norm(int norm, const void *r_out, const void *out, const void *x, int64_t B, int64_t N,
+                        int64_t D, int64_t sxB, int64_t sxN, int64_t sxD, const void *gate, int64_t s_gate_b,
+                        int64_t s_gate_n, int64_t s_gate_d, const void *y, const void *scale, int64_t s_scale_b,
+                        int64_t s_scale_n, const void *shift, int64_t s_shift_b, int64_t s_shift_n, float eps,
+                        int dtype, uint32_t flags) {
+    if (dtype != ADALN_BF16 && dtype != ADALN_FP16) return ADALN_E_DTYPE;
+    if (flags & ~ADALN_FLAG_PDL) return ADALN_E_VALUE;
+    if (norm != ADALN_NORM_LAYER && norm != ADALN_NORM_RMS) return ADALN_E_VALUE;
+    if (!out || !x || !scale || !shift) return ADALN_E_NULL;
+    if (gate && (!y || !r_out)) return ADALN_E_NULL;
+    if (B < 1 || N < 1 || D < 4 || D > 65536 || D % 4 != 0) return ADALN_E_SHAPE;
+    if (B > ((int64_t)1 << 40) / N || B * N > ((int64_t)1 << 46) / D) return ADALN_E_SHAPE;
+    if (sxB < 0 || sxN < 0 || sxD < 0 || s_scale_b < 0 || s_scale_n < 0 || s_shift_b < 0 || s_shift_n < 0)
+        return ADALN_E_STRIDE;
+    if (!finite_nonneg(eps)) return ADALN_E_VALUE;
+    if (!al2(out) || !al2(x) || !al2(scale) || !al2(shift)) return ADALN_E_ALIGN;
+    const int64_t nb = 2 * B * N * D;
+    const bool x_contig = sxD == 1 && (N == 1 || sxN == D) && (B == 1 || sxB == N * D);
+    const int64_t x_bytes = extent(B, N, D, sxB, sxN, sxD);
+    const int64_t sc_bytes = extent(B, N, D, s_scale_b, s_scale_n, 1);
+    const int64_t sh_bytes = extent(B, N, D, s_shift_b, s_shift_n, 1);
+    if (overlap(out, nb, scale, sc_bytes) || overlap(out, nb, shift, sh_bytes)) return ADALN_E_OVERLAP;
+    if (!gate) {
+        if (overlap(out, nb, x, x_bytes) && !(out == x && x_contig)) return ADALN_E_OVERLAP;
+        return ADALN_OK;
+    }
+    if (s_gate_b < 0 || s_gate_n < 0 || (s_gate_d != 0 && s_gate_d != 1)) return ADALN_E_STRIDE;
+    if (!x_contig) return ADALN_E_STRIDE;
+    if (!al2(gate) || !al2(y) || !al2(r_out)) return ADALN_E_ALIGN;
+    const int64_t g_bytes = extent(B, N, D, s_gate_b, s_gate_n, s_gate_d);
+    if (overlap(out, nb, x, nb) || overlap(out, nb, y, nb) || overlap(out, nb, r_out, nb) ||
+        overlap(out, nb, gate, g_bytes))
+        return ADALN_E_OVERLAP;
+    if (overlap(r_out, nb, x, nb) && r_out != x) return ADALN_E_OVERLAP;
+    if (overlap(r_out, nb, y, nb) && r_out != y) return ADALN_E_OVERLAP;
+    if (overlap(r_out, nb, gate, g_bytes) || overlap(r_out, nb, scale, sc_bytes) ||
+        overlap(r_out, nb, shift, sh_bytes))
+        return ADALN_E_OVERLAP;
+    return ADALN_OK;
+}
+
+LnArgs norm_args(int norm, void *r_out, void *out, const void *x, int64_t B, int64_t N, int64_t D, int64_t sxB,
+                 int64_t sxN, int64_t sxD, const void *gate, int64_t s_gate_b, int64_t s_gate_n, int64_t s_gate_d,
+                 const void *y, const void *scale, int64_t s_scale_b, int64_t s_scale_n, const void *shift,
+                 int64_t s_shift_b, int64_t s_shift_n, float eps) {
+    LnArgs a{out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps};
+    a.s_scale_n = s_scale_n;
+    a.s_shift_n = s_shift_n;
+    a.norm = norm;
+    if (gate) {
+        a.gate = gate;
+        a.s_gate_b = s_gate_b;
+        a.s_gate_n = s_gate_n;
+        a.s_gate_d = s_gate_d;
+        a.y = y;
+        a.r_out = r_out;
+    }
+    return a;
+}
+
 adaln_status check_gelu(const void *out, const void *x, const void *bias, int64_t rows, int64_t width,
                         int dtype, uint32_t flags) {
     if (dtype != ADALN_BF16 && dtype != ADALN_FP16) return ADALN_E_DTYPE;
@@ -338,8 +406,75 @@ adaln_status adaln_residual_gate_ln_modulate(void *r_out, void *out, const void 
     DeviceInfo info;
     if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
     LnArgs a{out, x, B, N, D, N * D, D, 1, scale, s_scale_b, shift, s_shift_b, eps};
-    return finish_launch(launch_residual_gate_ln_modulate(a, y, gate, s_gate_b, r_out, dtype,
-                                                          (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+    a.gate = gate;
+    a.s_gate_b = s_gate_b;
+    a.y = y;
+    a.r_out = r_out;
+    return finish_launch(launch_norm_scale_shift(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+adaln_status adaln_can_norm_scale_shift(int norm, const void *r_out, const void *out, const void *x, int64_t B,
+                                        int64_t N, int64_t D, int64_t sxB, int64_t sxN, int64_t sxD,
+                                        const void *gate, int64_t s_gate_b, int64_t s_gate_n, int64_t s_gate_d,
+                                        const void *y, const void *scale, int64_t s_scale_b, int64_t s_scale_n,
+                                        const void *shift, int64_t s_shift_b, int64_t s_shift_n, float eps,
+                                        int dtype, uint32_t flags) {
+    return check_norm(norm, r_out, out, x, B, N, D, sxB, sxN, sxD, gate, s_gate_b, s_gate_n, s_gate_d, y, scale,
+                      s_scale_b, s_scale_n, shift, s_shift_b, s_shift_n, eps, dtype, flags);
+}
+
+int adaln_norm_scale_shift_variant(int norm, const void *r_out, const void *out, const void *x, int64_t B, int64_t N,
+                                   int64_t D, int64_t sxB, int64_t sxN, int64_t sxD, const void *gate,
+                                   int64_t s_gate_b, int64_t s_gate_n, int64_t s_gate_d, const void *y,
+                                   const void *scale, int64_t s_scale_b, int64_t s_scale_n, const void *shift,
+                                   int64_t s_shift_b, int64_t s_shift_n, float eps, int dtype, uint32_t flags) {
+    adaln_status st = check_norm(norm, r_out, out, x, B, N, D, sxB, sxN, sxD, gate, s_gate_b, s_gate_n, s_gate_d, y,
+                                 scale, s_scale_b, s_scale_n, shift, s_shift_b, s_shift_n, eps, dtype, flags);
+    if (st != ADALN_OK) return -(int)st;
+    const LnArgs a = norm_args(norm, (void *)r_out, (void *)out, x, B, N, D, sxB, sxN, sxD, gate, s_gate_b, s_gate_n,
+                               s_gate_d, y, scale, s_scale_b, s_scale_n, shift, s_shift_b, s_shift_n, eps);
+    const int path = ln_modulate_path(a);
+    if (path == LN_PATH_TOKENS) {
+        int dev;
+        DeviceInfo info;
+        if (current_device(&dev) == ADALN_OK && device_info(dev, &info) == ADALN_OK && ln_tokens_tma_ready(a, info))
+            return LN_PATH_TOKENS_TMA;
+    }
+    return path;
+}
+
+adaln_status adaln_norm_scale_shift(int norm, void *r_out, void *out, const void *x, int64_t B, int64_t N, int64_t D,
+                                    int64_t sxB, int64_t sxN, int64_t sxD, const void *gate, int64_t s_gate_b,
+                                    int64_t s_gate_n, int64_t s_gate_d, const void *y, const void *scale,
+                                    int64_t s_scale_b, int64_t s_scale_n, const void *shift, int64_t s_shift_b,
+                                    int64_t s_shift_n, float eps, int dtype, uint32_t flags, void *stream) {
+    adaln_status st = check_norm(norm, r_out, out, x, B, N, D, sxB, sxN, sxD, gate, s_gate_b, s_gate_n, s_gate_d, y,
+                                 scale, s_scale_b, s_scale_n, shift, s_shift_b, s_shift_n, eps, dtype, flags);
+    if (st != ADALN_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
+    const LnArgs a = norm_args(norm, r_out, out, x, B, N, D, sxB, sxN, sxD, gate, s_gate_b, s_gate_n, s_gate_d, y,
+                               scale, s_scale_b, s_scale_n, shift, s_shift_b, s_shift_n, eps);
+    return finish_launch(launch_norm_scale_shift(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+adaln_status adaln_can_rmsnorm_scale_shift(const void *out, const void *x, int64_t B, int64_t N, int64_t D,
+                                           int64_t sxB, int64_t sxN, int64_t sxD, const void *scale,
+                                           int64_t s_scale_b, int64_t s_scale_n, const void *shift,
+                                           int64_t s_shift_b, int64_t s_shift_n, float eps, int dtype,
+                                           uint32_t flags) {
+    return check_norm(ADALN_NORM_RMS, nullptr, out, x, B, N, D, sxB, sxN, sxD, nullptr, 0, 0, 1, nullptr, scale,
+                      s_scale_b, s_scale_n, shift, s_shift_b, s_shift_n, eps, dtype, flags);
+}
+
+adaln_status adaln_rmsnorm_scale_shift(void *out, const void *x, int64_t B, int64_t N, int64_t D, int64_t sxB,
+                                       int64_t sxN, int64_t sxD, const void *scale, int64_t s_scale_b,
+                                       int64_t s_scale_n, const void *shift, int64_t s_shift_b, int64_t s_shift_n,
+                                       float eps, int dtype, uint32_t flags, void *stream) {
+    return adaln_norm_scale_shift(ADALN_NORM_RMS, nullptr, out, x, B, N, D, sxB, sxN, sxD, nullptr, 0, 0, 1, nullptr,
+                                  scale, s_scale_b, s_scale_n, shift, s_shift_b, s_shift_n, eps, dtype, flags,
+                                  stream);
 }
 
 adaln_status adaln_can_qk_head_layernorm(const void *q_out, const void *q, int64_t rows_q, const void *k_out,
@@ -359,6 +494,25 @@ adaln_status adaln_qk_head_layernorm(void *q_out, const void *q, int64_t rows_q,
     DeviceInfo info;
     if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
     QkArgs a{q_out, q, rows_q, k_out, k, rows_k, Dh, wq, bq, wk, bk, eps};
+    return finish_launch(
+        launch_qk_head_layernorm(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+adaln_status adaln_can_qk_rmsnorm(const void *q_out, const void *q, int64_t rows_q, const void *k_out,
+                                  const void *k, int64_t rows_k, int64_t Dh, const void *wq, const void *wk,
+                                  float eps, int dtype, uint32_t flags) {
+    return check_qk(q_out, q, rows_q, k_out, k, rows_k, Dh, wq, wq, wk, wk, eps, dtype, flags);
+}
+
+adaln_status adaln_qk_rmsnorm(void *q_out, const void *q, int64_t rows_q, void *k_out, const void *k,
+                              int64_t rows_k, int64_t Dh, const void *wq, const void *wk, float eps, int dtype,
+                              uint32_t flags, void *stream) {
+    adaln_status st = check_qk(q_out, q, rows_q, k_out, k, rows_k, Dh, wq, wq, wk, wk, eps, dtype, flags);
+    if (st != ADALN_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
+    QkArgs a{q_out, q, rows_q, k_out, k, rows_k, Dh, wq, nullptr, wk, nullptr, eps, true};
     return finish_launch(
         launch_qk_head_layernorm(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
 }

@@ -164,6 +164,12 @@ __device__ __forceinline__ void ld_stream32(uint32_t *r, const void *p) {
 __device__ __forceinline__ void ld_keep8(uint32_t *r, const void *p) {
     asm("ld.global.nc.v2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "l"(p));
 }
+// one 16-bit value (a per-token gate), zero-extended
+__device__ __forceinline__ uint32_t ldg_u16(const uint16_t *p) {
+    unsigned short v;
+    asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ void ld_keep16(uint32_t *r, const void *p) {
     asm("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "l"(p));

@@ -13,6 +13,9 @@ struct DeviceInfo {
     int l2_bytes = 0;
 };
 
+// One norm + modulate call: out = norm(v) * (1 + scale) + shift with v = x,
+// or v = x + gate * y (written to r_out) when gate is set.  The fields after
+// eps default to LayerNorm with one scale / shift row per sample and no gate.
 struct LnArgs {
     void *out;
     const void *x;
@@ -22,6 +25,12 @@ struct LnArgs {
     const void *shift;
     int64_t s_shift_b;
     float eps;
+    int64_t s_scale_n = 0, s_shift_n = 0;  // per-token operand rows (0: one row per sample)
+    int norm = 0;                          // 0 LayerNorm, 1 RMSNorm (both without affine)
+    const void *gate = nullptr;            // residual gate (b, n, d) at b*s_gate_b + n*s_gate_n + d*s_gate_d
+    int64_t s_gate_b = 0, s_gate_n = 0, s_gate_d = 1;
+    const void *y = nullptr;               // with a gate: y and r_out contiguous (B, N, D), x too
+    void *r_out = nullptr;
 };
 
 struct QkArgs {
@@ -32,8 +41,9 @@ struct QkArgs {
     const void *k;
     int64_t rows_k;
     int64_t Dh;
-    const void *wq, *bq, *wk, *bk;
+    const void *wq, *bq, *wk, *bk;  // RMSNorm: bq, bk unused
     float eps;
+    bool rms = false;               // per-head RMSNorm with a weight instead of LayerNorm with affine
 };
 
 struct GateArgs {
@@ -67,10 +77,9 @@ cudaError_t launch_qk_head_layernorm(const QkArgs &a, int dtype, bool pdl, cudaS
                                      const DeviceInfo &dev);
 cudaError_t launch_residual_gate_add(const GateArgs &a, int dtype, bool pdl, cudaStream_t s,
                                      const DeviceInfo &dev);
-// r = x + gate * y, out = LN(r) * (1 + scale) + shift; a.x is x (contiguous)
-bool residual_ln_fused_ok(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b, const void *r_out);
-cudaError_t launch_residual_gate_ln_modulate(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b,
-                                             void *r_out, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);
+// norm + modulate with every option of LnArgs (RMSNorm, per-token rows, a
+// residual gate); launch_ln_modulate is the same call
+cudaError_t launch_norm_scale_shift(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 cudaError_t launch_bias_gelu_tanh(const GeluArgs &a, int dtype, bool pdl, cudaStream_t s,
                                   const DeviceInfo &dev);
 cudaError_t launch_gelu_table_init(void *table, int dtype, cudaStream_t s);

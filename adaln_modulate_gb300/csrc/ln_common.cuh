@@ -167,6 +167,24 @@ __device__ __forceinline__ void fold128_s8(f2_t m01, f2_t q01, f2_t m23, f2_t q2
     m2 = q0;
 }
 
+// RMSNorm: the 128 lanes' sums of squares folded in the butterfly order of
+// fold128_s8 (offsets 16 and 8 inside the thread, then 4, 2, 1, 64, 32
+// across threads) with plain additions.  IEEE addition commutes, so both
+// partners of a stage compute the same bits.  Returned in every thread.
+__device__ __forceinline__ float fold128_sum_s8(f2_t s01, f2_t s23) {
+    float a, b;
+    f2_split(f2_add(s01, s23), a, b);  // offset 16: (s0 + s2, s1 + s3)
+    float t = __fadd_rn(a, b);         // offset 8
+    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 4));
+    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 2));
+    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 1));
+    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 16));  // offset 64
+    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 8));   // offset 32
+    return t;
+}
+
+// rstd = rsqrt_rn(m2 / D + eps): var = m2 / D for the LayerNorm, and with
+// m2 the sum of squares, ms = ss / D for the RMSNorm
 __device__ __forceinline__ float finish_rstd(float m2, float Df, float eps) {
     return rsqrt_rn(__fadd_rn(__fdiv_rn(m2, Df), eps));
 }
@@ -178,13 +196,18 @@ static inline bool ln_mult(int64_t v, int64_t a) { return v % a == 0; }
 bool ln_rows_ok(const LnArgs &a);
 constexpr int kRowsMaxNI = 8;     // contiguous rows in registers: D <= 4096
 constexpr int kTokensMaxNI = 12;  // tokens tile in shared memory: D <= 6144
-cudaError_t ln_rows_bf16(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev);
-cudaError_t ln_rows_fp16(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev);
-// residual gate-add fused in front of the LayerNorm (x, y, r_out, out contiguous)
-cudaError_t ln_rows_gate_bf16(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b, void *r_out,
-                              bool pdl, cudaStream_t s, const DeviceInfo &dev);
-cudaError_t ln_rows_gate_fp16(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b, void *r_out,
-                              bool pdl, cudaStream_t s, const DeviceInfo &dev);
+// contiguous-rows kernels (ln_rows_*.cu): LayerNorm / RMSNorm, without or
+// with the residual gate (a.gate; x, y, r_out, out contiguous)
+#define ADALN_ROWS_DECL(name) cudaError_t name(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev);
+ADALN_ROWS_DECL(rows_ln_bf16)
+ADALN_ROWS_DECL(rows_ln_fp16)
+ADALN_ROWS_DECL(rows_ln_gate_bf16)
+ADALN_ROWS_DECL(rows_ln_gate_fp16)
+ADALN_ROWS_DECL(rows_rms_bf16)
+ADALN_ROWS_DECL(rows_rms_fp16)
+ADALN_ROWS_DECL(rows_rms_gate_bf16)
+ADALN_ROWS_DECL(rows_rms_gate_fp16)
+#undef ADALN_ROWS_DECL
 cudaError_t ln_tokens_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 cudaError_t ln_generic_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 

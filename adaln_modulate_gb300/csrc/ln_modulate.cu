@@ -20,59 +20,64 @@
 //                     shared memory, writes the output contiguous;
 //   ln_generic_kernel any strides, one CTA of 128 threads per row, scalar
 //                     loads; the arithmetic is plain binary32 code.
+//
+// The same kernels serve the RMSNorm chain (rmsnorm_scale_shift of the
+// Normalization table: the lanes sum squares instead of running Welford,
+// the output pass is the LayerNorm's with mean 0), per-token modulation
+// rows (the strided [B, S, 6D] chunk views of the request-gated fusion
+// table) and the residual gate-add in front (scale_residual_norm_scale_shift,
+// with a per-sample gate row or a per-token [B, S, 1] gate); the tokens
+// kernels take only the LayerNorm with per-sample rows and no gate.
 #include "ln_common.cuh"
 
 namespace adaln {
 
 // The contiguous-rows kernel moves every logical lane's vec4 chunk with one
-// 8-byte access, so every row start of x, out, scale and shift must be
-// 8-byte aligned.  Strides of size-1 dimensions are never used and are
-// ignored.
+// 8-byte access, so every row start of x, out, scale and shift (and with a
+// gate of y, r_out and the gate rows) must be 8-byte aligned.  Strides of
+// size-1 dimensions are never used and are ignored.
 bool ln_rows_ok(const LnArgs &a) {
-    return ln_aligned(a.x, 8) && ln_aligned(a.out, 8) && ln_aligned(a.scale, 8) && ln_aligned(a.shift, 8) &&
-           (a.N == 1 || ln_mult(a.sxN, 4)) &&
-           (a.B == 1 || (ln_mult(a.sxB, 4) && ln_mult(a.s_scale_b, 4) && ln_mult(a.s_shift_b, 4)));
+    const bool base = ln_aligned(a.x, 8) && ln_aligned(a.out, 8) && ln_aligned(a.scale, 8) &&
+                      ln_aligned(a.shift, 8) && (a.N == 1 || ln_mult(a.sxN, 4)) &&
+                      (a.B == 1 || (ln_mult(a.sxB, 4) && ln_mult(a.s_scale_b, 4) && ln_mult(a.s_shift_b, 4))) &&
+                      (a.N == 1 || (ln_mult(a.s_scale_n, 4) && ln_mult(a.s_shift_n, 4)));
+    if (!base || !a.gate) return base;
+    if (!ln_aligned(a.y, 8) || !ln_aligned(a.r_out, 8)) return false;
+    // a per-token scalar gate is read one value at a time
+    return a.s_gate_d == 0 || (ln_aligned(a.gate, 8) && (a.B == 1 || ln_mult(a.s_gate_b, 4)) &&
+                               (a.N == 1 || ln_mult(a.s_gate_n, 4)));
 }
 
 int ln_modulate_path(const LnArgs &a) {
     const int64_t ni = (a.D + 511) / 512;
     if (a.sxD == 1 && ni <= kRowsMaxNI && ln_rows_ok(a)) return LN_PATH_ROWS;
-    // tokens contiguous: each d-row of 8 tokens is one 16-byte copy
-    if (a.sxN == 1 && a.sxD != 1 && a.N > 1 && ni <= kTokensMaxNI && ln_aligned(a.x, 16) &&
-        ln_mult(a.sxD, 8) && (a.B == 1 || (ln_mult(a.sxB, 8) && ln_mult(a.s_scale_b, 4) && ln_mult(a.s_shift_b, 4))) &&
+    // tokens contiguous (LayerNorm, one scale / shift row per sample, no
+    // gate): each d-row of 8 tokens is one 16-byte copy
+    const bool per_sample = a.s_scale_n == 0 && a.s_shift_n == 0;
+    if (a.norm == 0 && !a.gate && per_sample && a.sxN == 1 && a.sxD != 1 && a.N > 1 && ni <= kTokensMaxNI &&
+        ln_aligned(a.x, 16) && ln_mult(a.sxD, 8) &&
+        (a.B == 1 || (ln_mult(a.sxB, 8) && ln_mult(a.s_scale_b, 4) && ln_mult(a.s_shift_b, 4))) &&
         ln_aligned(a.out, 8) && ln_aligned(a.scale, 8) && ln_aligned(a.shift, 8))
         return LN_PATH_TOKENS;
     return LN_PATH_GENERIC;
 }
 
-cudaError_t launch_ln_modulate(const LnArgs &a, int dtype, bool pdl, cudaStream_t s,
-                               const DeviceInfo &dev) {
+cudaError_t launch_norm_scale_shift(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     switch (ln_modulate_path(a)) {
-        case LN_PATH_ROWS: return dtype == 0 ? ln_rows_bf16(a, pdl, s, dev) : ln_rows_fp16(a, pdl, s, dev);
+        case LN_PATH_ROWS: {
+            using RowsFn = cudaError_t (*)(const LnArgs &, bool, cudaStream_t, const DeviceInfo &);
+            static const RowsFn fns[2][2][2] = {  // [norm][gate][dtype]
+                {{rows_ln_bf16, rows_ln_fp16}, {rows_ln_gate_bf16, rows_ln_gate_fp16}},
+                {{rows_rms_bf16, rows_rms_fp16}, {rows_rms_gate_bf16, rows_rms_gate_fp16}}};
+            return fns[a.norm == 1][a.gate != nullptr][dtype != 0](a, pdl, s, dev);
+        }
         case LN_PATH_TOKENS: return ln_tokens_launch(a, dtype, pdl, s, dev);
         default: return ln_generic_launch(a, dtype, pdl, s, dev);
     }
 }
 
-// The fused kernel when the rows path takes these rows and y, r_out and the
-// gate rows are 8-byte aligned with strides that keep them so; otherwise the
-// gate-add kernel writes r and the LayerNorm reads it back (two launches).
-bool residual_ln_fused_ok(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b, const void *r_out) {
-    return ln_modulate_path(a) == LN_PATH_ROWS && ln_aligned(y, 8) && ln_aligned(r_out, 8) && ln_aligned(gate, 8) &&
-           (a.B == 1 || ln_mult(s_gate_b, 4));
-}
-
-cudaError_t launch_residual_gate_ln_modulate(const LnArgs &a, const void *y, const void *gate, int64_t s_gate_b,
-                                             void *r_out, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    if (residual_ln_fused_ok(a, y, gate, s_gate_b, r_out))
-        return dtype == 0 ? ln_rows_gate_bf16(a, y, gate, s_gate_b, r_out, pdl, s, dev)
-                          : ln_rows_gate_fp16(a, y, gate, s_gate_b, r_out, pdl, s, dev);
-    const GateArgs g{r_out, a.x, gate, s_gate_b, y, a.B, a.N, a.D};
-    cudaError_t e = launch_residual_gate_add(g, dtype, pdl, s, dev);
-    if (e != cudaSuccess) return e;
-    LnArgs ln = a;
-    ln.x = r_out;
-    return launch_ln_modulate(ln, dtype, pdl, s, dev);
+cudaError_t launch_ln_modulate(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    return launch_norm_scale_shift(a, dtype, pdl, s, dev);
 }
 
 }  // namespace adaln

@@ -1,7 +1,7 @@
-// Contiguous-rows kernel of ln_modulate (one warp per row); instantiated per
-// storage type in ln_rows_bf16.cu / ln_rows_fp16.cu.  Every global access is
-// 8 bytes (one logical lane's vec4 chunk), so rows only need 8-byte aligned
-// starts.
+// Contiguous-rows kernel of the norm + modulate chains (one warp per row);
+// instantiated per storage type, norm and gate in ln_rows_*.cu (eight
+// translation units that compile in parallel).  Every global access of a row is 8 bytes (one
+// logical lane's vec4 chunk), so rows only need 8-byte aligned starts.
 #pragma once
 #include "ln_common.cuh"
 
@@ -20,38 +20,60 @@ constexpr int kRowsThreads = 256;
 // not a multiple of 512 (the last step masks lanes past D/4 and the fold
 // coefficients are computed per thread).
 //
+// RMS: RMSNorm instead of LayerNorm.  Each lane sums x*x over its chunks
+// (square and sum rounded separately), the same butterfly folds the sums
+// with plain additions, rstd = rsqrt_rn(ss / D + eps), and the output pass
+// is the LayerNorm's with mean 0 (x - 0 is x exactly).  Masked tail lanes
+// hold zeros, which add nothing.
+//
 // OPSH: the modulate operands op = round(1 + scale) and shift of all B
 // samples are computed once per CTA into shared memory (B * D * 4 bytes, at
 // most kOpshMaxBytes), interleaved per column pair as (op, shift), so the
 // output pass reads one 16-byte shared word per lane chunk instead of two
 // global loads and an add per column pair.  Otherwise scale and shift are
-// read from global memory (L2) in the output pass.
+// read from global memory (L2) in the output pass, at
+// b * s_scale_b + n * s_scale_n (per-token rows, e.g. the chunks of a
+// [B, S, 6D] modulation table, have s_scale_n != 0 and never use the table).
 constexpr int kOpshMaxBytes = 32 * 1024;
 
-// GATE: the row is first r = round(x + round(gate * y)) (the residual
-// gate-add chain, x and y contiguous), written to r_out, and the LayerNorm
-// and modulate run on r: one read of x and y, one write of r and out.
-// With OPSH the gate rows join the shared table (after the op / shift
-// pairs, B * D * 2 more bytes; the whole table stays within kOpshMaxBytes).
-struct RowsGate {
+// GM (gate mode): with a gate (GM != GATE_NONE) the row is first
+// r = round(x + round(gate * y)) (the residual gate-add chain, x and y
+// contiguous), written to r_out, and the norm and modulate run on r: one
+// read of x and y, one write of r and out.  The gate of (b, n) sits at
+// b * s_gate_b + n * s_gate_n: a row (GATE_ROW) or one value (GATE_SCALAR,
+// a per-token [B, S, 1] gate).  GATE_ROW with OPSH: the rows are one per
+// sample and join the shared table after the op / shift pairs (B * D * 2
+// more bytes; the whole table stays within kOpshMaxBytes).
+enum GateMode : int { GATE_NONE = 0, GATE_ROW = 1, GATE_SCALAR = 2 };
+struct RowsParams {
+    uint16_t *out;
+    const uint16_t *x;
+    int64_t rows, B, N;
+    int D;
+    int64_t sxB, sxN;
+    const uint16_t *scale;
+    int64_t s_scale_b, s_scale_n;
+    const uint16_t *shift;
+    int64_t s_shift_b, s_shift_n;
+    float eps;
     const uint16_t *y;
     const uint16_t *gate;
-    int64_t s_gate_b;
+    int64_t s_gate_b, s_gate_n;
     uint16_t *r_out;
 };
 
-template <DT T, int NI, bool TAIL, bool OPSH, bool GATE>
+template <DT T, int NI, bool TAIL, bool OPSH, int GM, bool RMS>
 __global__ void __launch_bounds__(kRowsThreads, 2)
-ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_t N, int D,
-               int64_t sxB, int64_t sxN, const uint16_t *scale, int64_t s_scale_b,
-               const uint16_t *shift, int64_t s_shift_b, float eps, RowsGate g) {
-    extern __shared__ __align__(16) uint32_t opsh[];  // OPSH: [b][column pair][op, shift] (+ GATE: [b][pair] gate)
+ln_rows_kernel(const RowsParams p) {
+    constexpr bool GATE = GM != GATE_NONE;
+    constexpr bool GTAB = OPSH && GM == GATE_ROW;      // gate rows in the shared table
+    extern __shared__ __align__(16) uint32_t opsh[];  // OPSH: [b][column pair][op, shift] (+ GTAB: [b][pair] gate)
     // this CTA's rows, from launch parameters only: computed before waiting
     // on the previous kernel and passed through shared memory so that the
     // parameter reads (a constant-cache miss) stay ahead of the wait
     __shared__ int64_t cta_rows[2];
     if (threadIdx.x == 0) {
-        const int64_t per = rows / gridDim.x, extra = rows % gridDim.x;
+        const int64_t per = p.rows / gridDim.x, extra = p.rows % gridDim.x;
         cta_rows[0] = blockIdx.x * per + imin64(blockIdx.x, extra);
         cta_rows[1] = cta_rows[0] + per + (blockIdx.x < extra ? 1 : 0);
     }
@@ -60,16 +82,20 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
     pdl_trigger();
     const int u = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int D = p.D;
+    const int64_t N = p.N;
     const int nvec = D >> 2;
     const float Df = (float)D;
     const int l0 = (u & 7) + 32 * (u >> 3);
     const int c0 = 4 * l0;  // element offset of lane l0 at step 0
 
     FoldPlan plan;
-    if constexpr (TAIL) {
-        plan = fold_plan_runtime(u, nvec);
-    } else {
-        plan = fold_plan_uniform(NI);
+    if constexpr (!RMS) {
+        if constexpr (TAIL) {
+            plan = fold_plan_runtime(u, nvec);
+        } else {
+            plan = fold_plan_uniform(NI);
+        }
     }
     bool vlast[4];
 #pragma unroll
@@ -83,7 +109,7 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
     uint32_t xv[NI][4][2];
     auto load_row = [&](int64_t row) {
         const int64_t b = row / N;
-        const uint16_t *xr = x + b * sxB + (row - b * N) * sxN + c0;
+        const uint16_t *xr = p.x + b * p.sxB + (row - b * N) * p.sxN + c0;
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
 #pragma unroll
@@ -102,7 +128,7 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
     if constexpr (OPSH) {
         // all loads of a batch in flight before any is used
         constexpr int kFill = 8;
-        const int half = D / 2, npairs = (int)B * half;  // npairs <= kOpshMaxBytes / 8
+        const int half = D / 2, npairs = (int)p.B * half;  // npairs <= kOpshMaxBytes / 8
         for (int base = 0; base < npairs; base += kFill * kRowsThreads) {
             uint32_t s2[kFill], h2[kFill], g2[kFill];
 #pragma unroll
@@ -110,10 +136,10 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
                 const int e = base + k * kRowsThreads + threadIdx.x;
                 if (e < npairs) {
                     const int bb = e / half, cp = e - bb * half;
-                    asm("ld.global.nc.b32 %0, [%1];" : "=r"(s2[k]) : "l"(scale + bb * s_scale_b + 2 * cp));
-                    asm("ld.global.nc.b32 %0, [%1];" : "=r"(h2[k]) : "l"(shift + bb * s_shift_b + 2 * cp));
-                    if constexpr (GATE)
-                        asm("ld.global.nc.b32 %0, [%1];" : "=r"(g2[k]) : "l"(g.gate + bb * g.s_gate_b + 2 * cp));
+                    asm("ld.global.nc.b32 %0, [%1];" : "=r"(s2[k]) : "l"(p.scale + bb * p.s_scale_b + 2 * cp));
+                    asm("ld.global.nc.b32 %0, [%1];" : "=r"(h2[k]) : "l"(p.shift + bb * p.s_shift_b + 2 * cp));
+                    if constexpr (GTAB)
+                        asm("ld.global.nc.b32 %0, [%1];" : "=r"(g2[k]) : "l"(p.gate + bb * p.s_gate_b + 2 * cp));
                 }
             }
 #pragma unroll
@@ -122,7 +148,7 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
                 if (e < npairs) {
                     opsh[2 * e] = add16x2<T>(s2[k], one16x2<T>());
                     opsh[2 * e + 1] = h2[k];
-                    if constexpr (GATE) opsh[2 * npairs + e] = g2[k];
+                    if constexpr (GTAB) opsh[2 * npairs + e] = g2[k];
                 }
             }
         }
@@ -130,28 +156,38 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
     }
 
     for (; row < r1; row += kRowsThreads / 32) {
-        const int64_t b = row / N;
+        const int64_t b = row / N, n = row - b * N;
 
-        // pass 1: Welford of lanes (s0, s1) and (s2, s3), one f32x2 op each
+        // pass 1: Welford (or the sum of squares) of lanes (s0, s1) and
+        // (s2, s3), one f32x2 op each
         f2_t m01 = f2(0.f, 0.f), q01 = m01, m23 = m01, q23 = m01;
+        const uint16_t *gr = nullptr;  // GATE: this row's gate row (or value)
+        uint32_t gs = 0;               // GATE_SCALAR: the value in both halves
+        if constexpr (GATE) gr = p.gate + b * p.s_gate_b + n * p.s_gate_n;
+        if constexpr (GM == GATE_SCALAR) {
+            const uint32_t g1 = ldg_u16(gr);
+            gs = g1 | (g1 << 16);
+        }
         static_for<0, NI>([&](auto I) {
             constexpr int i = decltype(I)::value;
             if constexpr (GATE) {
                 // this step's chunks become r = round(x + round(gate * y)), stored
-                const uint16_t *yr = g.y + row * (int64_t)D + c0;
-                uint16_t *rr_out = g.r_out + row * (int64_t)D + c0;
+                const uint16_t *yr = p.y + row * (int64_t)D + c0;
+                uint16_t *rr_out = p.r_out + row * (int64_t)D + c0;
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
                     if (i < NI - 1 || vlast[s]) {
                         const int off = 512 * i + 32 * s;
                         uint32_t yv[2], gv[2];
                         ld_stream8(yv, yr + off);
-                        if constexpr (OPSH) {
-                            const uint2 t = *reinterpret_cast<const uint2 *>(opsh + 2 * (int)(B * (D / 2)) + b * (D / 2) + (c0 + off) / 2);
+                        if constexpr (GM == GATE_SCALAR) {
+                            gv[0] = gv[1] = gs;
+                        } else if constexpr (GTAB) {
+                            const uint2 t = *reinterpret_cast<const uint2 *>(opsh + 2 * (int)(p.B * (D / 2)) + b * (D / 2) + (c0 + off) / 2);
                             gv[0] = t.x;
                             gv[1] = t.y;
                         } else {
-                            ld_keep8(gv, g.gate + b * g.s_gate_b + c0 + off);
+                            ld_keep8(gv, gr + c0 + off);
                         }
                         xv[i][s][0] = add16x2<T>(xv[i][s][0], mul16x2<T>(gv[0], yv[0]));
                         xv[i][s][1] = add16x2<T>(xv[i][s][1], mul16x2<T>(gv[1], yv[1]));
@@ -161,12 +197,17 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
             }
             static_for<0, 4>([&](auto E) {
                 constexpr int e = decltype(E)::value;
-                constexpr float r = Rcp<4 * i + e + 1>::value;
+                [[maybe_unused]] constexpr float r = Rcp<4 * i + e + 1>::value;  // Welford 1/(count+1)
                 float a[4];
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     a[s] = (e & 1) ? hi_f32<T>(xv[i][s][e >> 1]) : lo_f32<T>(xv[i][s][e >> 1]);
-                if (!TAIL || i < NI - 1) {
+                if constexpr (RMS) {
+                    // masked tail lanes hold zeros: adding 0 * 0 keeps the sum
+                    const f2_t a01 = f2(a[0], a[1]), a23 = f2(a[2], a[3]);
+                    q01 = f2_add(q01, f2_mul(a01, a01));
+                    q23 = f2_add(q23, f2_mul(a23, a23));
+                } else if (!TAIL || i < NI - 1) {
                     push2(m01, q01, f2(a[0], a[1]), r);
                     push2(m23, q23, f2(a[2], a[3]), r);
                 } else {
@@ -200,18 +241,23 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
         // its DRAM reads overlap this row's fold, output pass and stores
         if (u == 0 && row + kRowsThreads / 32 < r1) {
             const int64_t rn = row + kRowsThreads / 32, bn = rn / N;
-            prefetch_l2(x + bn * sxB + (rn - bn * N) * sxN, (uint64_t)D * 2);
+            prefetch_l2(p.x + bn * p.sxB + (rn - bn * N) * p.sxN, (uint64_t)D * 2);
         }
 
         float mean, m2;
-        fold128_s8(m01, q01, m23, q23, plan, mean, m2);
-        const float rstd = finish_rstd(m2, Df, eps);
+        if constexpr (RMS) {
+            mean = 0.0f;
+            m2 = fold128_sum_s8(q01, q23);
+        } else {
+            fold128_s8(m01, q01, m23, q23, plan, mean, m2);
+        }
+        const float rstd = finish_rstd(m2, Df, p.eps);
 
         // pass 2: normalise, modulate, store
-        const uint16_t *scr = scale + b * s_scale_b + c0;
-        const uint16_t *shr = shift + b * s_shift_b + c0;
+        const uint16_t *scr = p.scale + b * p.s_scale_b + n * p.s_scale_n + c0;
+        const uint16_t *shr = p.shift + b * p.s_shift_b + n * p.s_shift_n + c0;
         const uint32_t *ob = opsh + b * D + c0;  // OPSH: (op, shift) of the column pairs from c0 on
-        uint16_t *orow = out + row * (int64_t)D + c0;
+        uint16_t *orow = p.out + row * (int64_t)D + c0;
         const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
@@ -249,51 +295,69 @@ ln_rows_kernel(uint16_t *out, const uint16_t *x, int64_t rows, int64_t B, int64_
     }
 }
 
-static inline int64_t rows_opsh_bytes(const LnArgs &a, bool gate) { return a.B * a.D * (gate ? 6 : 4); }
+// the op / shift table of all samples (and with GATE_ROW the gate rows) in
+// shared memory, in bytes
+static inline int64_t rows_opsh_bytes(const LnArgs &a, int gm) { return a.B * a.D * (gm == GATE_ROW ? 6 : 4); }
 
-template <DT T, int NI, bool TAIL, bool OPSH, bool GATE>
-static cudaError_t run_rows(const LnArgs &a, const RowsGate &g, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    auto k = ln_rows_kernel<T, NI, TAIL, OPSH, GATE>;
+// the op / shift rows (and with GATE_ROW the gate rows) are one per sample
+// and the table fits in shared memory (the rows path already guarantees
+// 8-byte aligned rows and even strides)
+static inline bool rows_opsh_ok(const LnArgs &a, int gm) {
+    const bool per_sample = a.N == 1 || (a.s_scale_n == 0 && a.s_shift_n == 0 && (gm != GATE_ROW || a.s_gate_n == 0));
+    return per_sample && rows_opsh_bytes(a, gm) <= kOpshMaxBytes;
+}
+
+static inline int rows_gate_mode(const LnArgs &a) {
+    return !a.gate ? GATE_NONE : (a.s_gate_d == 0 ? GATE_SCALAR : GATE_ROW);
+}
+
+template <DT T, int NI, bool TAIL, bool OPSH, int GM, bool RMS>
+static cudaError_t run_rows(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    auto k = ln_rows_kernel<T, NI, TAIL, OPSH, GM, RMS>;
     // <= kOpshMaxBytes with OPSH (rows_opsh_ok), which leaves room for the
     // static shared memory under the 48 KiB a launch gets without opt-in
-    const size_t smem = OPSH ? (size_t)rows_opsh_bytes(a, GATE) : 0;
+    const size_t smem = OPSH ? (size_t)rows_opsh_bytes(a, GM) : 0;
     const int64_t rows = a.B * a.N;
     const int64_t ctas_needed = (rows + kRowsThreads / 32 - 1) / (kRowsThreads / 32);
     const int64_t grid = imin64(ctas_needed, (int64_t)dev.sms * blocks_per_sm(k, kRowsThreads, smem));
-    return launch_k(k, dim3((unsigned)grid), dim3(kRowsThreads), smem, s, pdl, (uint16_t *)a.out,
-                    (const uint16_t *)a.x, rows, a.B, a.N, (int)a.D, a.sxB, a.sxN,
-                    (const uint16_t *)a.scale, a.s_scale_b, (const uint16_t *)a.shift, a.s_shift_b,
-                    a.eps, g);
+    RowsParams p{(uint16_t *)a.out, (const uint16_t *)a.x, rows, a.B, a.N, (int)a.D, a.sxB, a.sxN,
+                 (const uint16_t *)a.scale, a.s_scale_b, a.N == 1 ? 0 : a.s_scale_n,
+                 (const uint16_t *)a.shift, a.s_shift_b, a.N == 1 ? 0 : a.s_shift_n, a.eps,
+                 (const uint16_t *)a.y, (const uint16_t *)a.gate, a.s_gate_b, a.N == 1 ? 0 : a.s_gate_n,
+                 (uint16_t *)a.r_out};
+    return launch_k(k, dim3((unsigned)grid), dim3(kRowsThreads), smem, s, pdl, p);
 }
 
-// the op / shift table of all samples (and with GATE the gate rows) fits in
-// shared memory (the rows path already guarantees 8-byte aligned scale /
-// shift and even strides)
-static inline bool rows_opsh_ok(const LnArgs &a, bool gate) { return rows_opsh_bytes(a, gate) <= kOpshMaxBytes; }
-
-template <DT T, int NI, bool GATE>
-static cudaError_t rows_tail(const LnArgs &a, const RowsGate &g, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+template <DT T, int NI, int GM, bool RMS>
+static cudaError_t rows_tail(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     const bool tail = a.D % 512 != 0;
-    if (rows_opsh_ok(a, GATE))
-        return tail ? run_rows<T, NI, true, true, GATE>(a, g, pdl, s, dev)
-                    : run_rows<T, NI, false, true, GATE>(a, g, pdl, s, dev);
-    return tail ? run_rows<T, NI, true, false, GATE>(a, g, pdl, s, dev)
-                : run_rows<T, NI, false, false, GATE>(a, g, pdl, s, dev);
+    if (rows_opsh_ok(a, GM))
+        return tail ? run_rows<T, NI, true, true, GM, RMS>(a, pdl, s, dev)
+                    : run_rows<T, NI, false, true, GM, RMS>(a, pdl, s, dev);
+    return tail ? run_rows<T, NI, true, false, GM, RMS>(a, pdl, s, dev)
+                : run_rows<T, NI, false, false, GM, RMS>(a, pdl, s, dev);
 }
 
-template <DT T, bool GATE>
-static cudaError_t rows_vec(const LnArgs &a, const RowsGate &g, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+template <DT T, int GM, bool RMS>
+static cudaError_t rows_vec(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     switch ((a.D + 511) / 512) {
-        case 1: return rows_tail<T, 1, GATE>(a, g, pdl, s, dev);
-        case 2: return rows_tail<T, 2, GATE>(a, g, pdl, s, dev);
-        case 3: return rows_tail<T, 3, GATE>(a, g, pdl, s, dev);
-        case 4: return rows_tail<T, 4, GATE>(a, g, pdl, s, dev);
-        case 5: return rows_tail<T, 5, GATE>(a, g, pdl, s, dev);
-        case 6: return rows_tail<T, 6, GATE>(a, g, pdl, s, dev);
-        case 7: return rows_tail<T, 7, GATE>(a, g, pdl, s, dev);
-        case 8: return rows_tail<T, 8, GATE>(a, g, pdl, s, dev);
+        case 1: return rows_tail<T, 1, GM, RMS>(a, pdl, s, dev);
+        case 2: return rows_tail<T, 2, GM, RMS>(a, pdl, s, dev);
+        case 3: return rows_tail<T, 3, GM, RMS>(a, pdl, s, dev);
+        case 4: return rows_tail<T, 4, GM, RMS>(a, pdl, s, dev);
+        case 5: return rows_tail<T, 5, GM, RMS>(a, pdl, s, dev);
+        case 6: return rows_tail<T, 6, GM, RMS>(a, pdl, s, dev);
+        case 7: return rows_tail<T, 7, GM, RMS>(a, pdl, s, dev);
+        case 8: return rows_tail<T, 8, GM, RMS>(a, pdl, s, dev);
     }
     return cudaErrorInvalidValue;
+}
+
+// the two gate forms of one (storage type, norm)
+template <DT T, bool RMS>
+static cudaError_t rows_gated(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    return rows_gate_mode(a) == GATE_SCALAR ? rows_vec<T, GATE_SCALAR, RMS>(a, pdl, s, dev)
+                                            : rows_vec<T, GATE_ROW, RMS>(a, pdl, s, dev);
 }
 
 }  // namespace adaln

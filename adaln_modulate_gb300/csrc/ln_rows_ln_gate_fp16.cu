@@ -1,0 +1,10 @@
+// LayerNorm contiguous-rows kernels, fp16 storage, with the residual gate-add in front.
+#include "ln_rows.cuh"
+
+namespace adaln {
+
+cudaError_t rows_ln_gate_fp16(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    return rows_gated<DT::FP16, false>(a, pdl, s, dev);
+}
+
+}  // namespace adaln

@@ -1,0 +1,10 @@
+// RMSNorm contiguous-rows kernels, bf16 storage, with the residual gate-add in front.
+#include "ln_rows.cuh"
+
+namespace adaln {
+
+cudaError_t rows_rms_gate_bf16(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
+    return rows_gated<DT::BF16, true>(a, pdl, s, dev);
+}
+
+}  // namespace adaln

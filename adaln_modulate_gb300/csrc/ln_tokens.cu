@@ -186,57 +186,6 @@ ln_tokens_kernel(uint16_t *out, const uint16_t *x, int64_t N, int D, int64_t sxB
     }
 }
 
-// ---------------------------------------------------------------------
-// any strides: one CTA of 128 threads per row, plain binary32 code
-// ---------------------------------------------------------------------
-
-template <DT T>
-__global__ void __launch_bounds__(128)
-ln_generic_kernel(uint16_t *out, const uint16_t *x, int64_t B, int64_t N, int64_t D, int64_t sxB,
-                  int64_t sxN, int64_t sxD, const uint16_t *scale, int64_t s_scale_b,
-                  const uint16_t *shift, int64_t s_shift_b, float eps) {
-    __shared__ float xch[4][3];
-    __shared__ float fin[2];
-    const int l = threadIdx.x;
-    const int64_t nvec = D >> 2;
-    const float Df = (float)D;
-    pdl_wait();
-    pdl_trigger();
-    for (int64_t row = blockIdx.x; row < B * N; row += gridDim.x) {
-        const int64_t b = row / N, n = row - b * N;
-        const uint16_t *xr = x + b * sxB + n * sxN;
-        Stat s{0.f, 0.f, 0.f};
-        for (int64_t j = l; j < nvec; j += 128)
-            for (int e = 0; e < 4; ++e) push1(s, h_f32<T>(xr[(4 * j + e) * sxD]));
-        for (int off = 16; off >= 1; off >>= 1) s = shfl_stage(s, off);
-        if ((l & 31) == 0) {
-            xch[l >> 5][0] = s.mean;
-            xch[l >> 5][1] = s.m2;
-            xch[l >> 5][2] = s.cnt;
-        }
-        __syncthreads();
-        if (l == 0) {
-            Stat g[4];
-            for (int w = 0; w < 4; ++w) g[w] = Stat{xch[w][0], xch[w][1], xch[w][2]};
-            const Stat f = chan(chan(g[0], g[2]), chan(g[1], g[3]));
-            fin[0] = f.mean;
-            fin[1] = finish_rstd(f.m2, Df, eps);
-        }
-        __syncthreads();
-        const float mean = fin[0], rstd = fin[1];
-        const uint16_t *scr = scale + b * s_scale_b, *shr = shift + b * s_shift_b;
-        uint16_t *orow = out + row * D;
-        for (int64_t d = l; d < D; d += 128) {
-            const float v = h_f32<T>(xr[d * sxD]);
-            const float y = h_f32<T>(to16_rn<T>(__fmul_rn(rstd, __fsub_rn(v, mean))));
-            const float op = h_f32<T>(to16_rn<T>(__fadd_rn(1.0f, h_f32<T>(scr[d]))));
-            const float p = h_f32<T>(to16_rn<T>(__fmul_rn(y, op)));
-            orow[d] = to16_rn<T>(__fadd_rn(p, h_f32<T>(shr[d])));
-        }
-        __syncthreads();
-    }
-}
-
 template <DT T, int NI>
 static cudaError_t run_tokens(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     auto k = ln_tokens_kernel<T, NI>;
@@ -275,27 +224,12 @@ static cudaError_t tokens_ni(const LnArgs &a, bool pdl, cudaStream_t s, const De
     return cudaErrorInvalidValue;
 }
 
-template <DT T>
-static cudaError_t run_generic(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    auto k = ln_generic_kernel<T>;
-    const int64_t rows = a.B * a.N;
-    const int64_t grid = imin64(rows, (int64_t)dev.sms * blocks_per_sm(k, 128, 0));
-    return launch_k(k, dim3((unsigned)grid), dim3(128), 0, s, pdl, (uint16_t *)a.out,
-                    (const uint16_t *)a.x, a.B, a.N, a.D, a.sxB, a.sxN, a.sxD,
-                    (const uint16_t *)a.scale, a.s_scale_b, (const uint16_t *)a.shift, a.s_shift_b,
-                    a.eps);
-}
-
 cudaError_t ln_tokens_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     if (ln_tokens_tma_fits(a, dev)) {
         const cudaError_t e = ln_tokens_tma_launch(a, dtype, pdl, s, dev);
         if (e != cudaErrorNotSupported) return e;
     }
     return dtype == 0 ? tokens_ni<DT::BF16>(a, pdl, s, dev) : tokens_ni<DT::FP16>(a, pdl, s, dev);
-}
-
-cudaError_t ln_generic_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    return dtype == 0 ? run_generic<DT::BF16>(a, pdl, s, dev) : run_generic<DT::FP16>(a, pdl, s, dev);
 }
 
 }  // namespace adaln

@@ -18,6 +18,12 @@
 // Chan's coefficients depend only on Dh (lanes past Dh/4 hold nothing); for
 // Dh = 128 they are 1/2 with the lower count 4, 8, 16, 32, 64.  The affine
 // (w, b) of q and of k are staged in shared memory as binary32.
+//
+// RMS: the per-head QK RMSNorm of the same page (qk_rmsnorm_native): each
+// lane sums x*x (square and sum rounded separately), the same butterfly
+// folds the sums with plain additions, rstd = rsqrt_rn(ss / Dh + eps),
+// u = rstd * x and out = round(w * u) (binary32 product, one storage
+// rounding); there is no bias.
 #include "common.cuh"
 #include "kernels.h"
 #include "ln_common.cuh"
@@ -41,7 +47,7 @@ __host__ __device__ constexpr float qk_coef(int l, int o, int nl) {
 
 // NL: logical lanes holding data (Dh / 4) as a compile-time constant (all
 // fold coefficients are then constants), or 0 for a run-time Dh.
-template <DT T, int NL>
+template <DT T, int NL, bool RMS>
 __global__ void __launch_bounds__(kQkThreads)
 qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out,
              const uint16_t *k, int64_t rows_k, int Dh, const uint16_t *wq, const uint16_t *bq,
@@ -54,9 +60,9 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
     for (int c = threadIdx.x; c < 128; c += kQkThreads) {
         const bool in = c < Dh;
         aff[0][0][c] = (in && rows_q) ? h_f32<T>(wq[c]) : 0.0f;
-        aff[0][1][c] = (in && rows_q) ? h_f32<T>(bq[c]) : 0.0f;
+        aff[0][1][c] = (!RMS && in && rows_q) ? h_f32<T>(bq[c]) : 0.0f;
         aff[1][0][c] = (in && rows_k) ? h_f32<T>(wk[c]) : 0.0f;
-        aff[1][1][c] = (in && rows_k) ? h_f32<T>(bk[c]) : 0.0f;
+        aff[1][1][c] = (!RMS && in && rows_k) ? h_f32<T>(bk[c]) : 0.0f;
     }
     __syncthreads();
 
@@ -80,12 +86,18 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
         }
 
         // Welford of every lane (counts 1..4) on lane pairs (2k, 2k+1);
-        // lanes at or past nl keep (0, 0)
+        // lanes at or past nl keep (0, 0).  RMS: the sums of squares in qq
         f2_t m[16], qq[16];
 #pragma unroll
         for (int kp = 0; kp < 16; ++kp) {
             m[kp] = qq[kp] = f2(0.f, 0.f);
-            if (2 * kp < nl) {
+            if (RMS && 2 * kp < nl) {
+                // the odd lane of a pair past the end holds zeros: it adds nothing
+                const uint32_t *a0 = v[2 * kp], *a1 = v[2 * kp + 1];
+                const f2_t e0 = f2(lo_f32<T>(a0[0]), lo_f32<T>(a1[0])), e1 = f2(hi_f32<T>(a0[0]), hi_f32<T>(a1[0]));
+                const f2_t e2 = f2(lo_f32<T>(a0[1]), lo_f32<T>(a1[1])), e3 = f2(hi_f32<T>(a0[1]), hi_f32<T>(a1[1]));
+                qq[kp] = f2_add(f2_add(f2_add(f2_mul(e0, e0), f2_mul(e1, e1)), f2_mul(e2, e2)), f2_mul(e3, e3));
+            } else if (!RMS && 2 * kp < nl) {
                 const uint32_t *a0 = v[2 * kp], *a1 = v[2 * kp + 1];
                 push2(m[kp], qq[kp], f2(lo_f32<T>(a0[0]), lo_f32<T>(a1[0])), Rcp<1>::value);
                 push2(m[kp], qq[kp], f2(hi_f32<T>(a0[0]), hi_f32<T>(a1[0])), Rcp<2>::value);
@@ -102,7 +114,17 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
         }
 
         float mean, m2;
-        if constexpr (NL != 0) {
+        if constexpr (RMS) {
+            // offsets 16, 8, 4, 2 on lane pairs, offset 1 on the two halves
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+                for (int kp = 0; kp < o; ++kp) qq[kp] = f2_add(qq[kp], qq[kp + o]);
+            float a0, a1;
+            f2_split(qq[0], a0, a1);
+            mean = 0.0f;
+            m2 = __fadd_rn(a0, a1);
+        } else if constexpr (NL != 0) {
             // offsets 16, 8, 4, 2 on lane pairs, offset 1 on the two halves
 #define QK_STAGE(O)                                                                  \
     _Pragma("unroll") for (int kp = 0; kp < (O) / 2; ++kp) {                         \
@@ -143,7 +165,7 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
         }
         const float rstd = rsqrt_rn(__fadd_rn(__fdiv_rn(m2, Df), eps));
 
-        // out = round(fma(w, rstd * (x - mean), b))
+        // out = round(fma(w, rstd * (x - mean), b)); RMS: round(w * (rstd * x))
         const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
         uint32_t o[32][2];
 #pragma unroll
@@ -156,8 +178,13 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
                 unpack_again<T>(v[l][1], x2, x3);
                 f2_t u01 = f2_mul(f2_sub(f2(x0, x1), mm), rr);
                 f2_t u23 = f2_mul(f2_sub(f2(x2, x3), mm), rr);
-                u01 = f2_fma(f2(w4.x, w4.y), u01, f2(b4.x, b4.y));
-                u23 = f2_fma(f2(w4.z, w4.w), u23, f2(b4.z, b4.w));
+                if constexpr (RMS) {
+                    u01 = f2_mul(f2(w4.x, w4.y), u01);
+                    u23 = f2_mul(f2(w4.z, w4.w), u23);
+                } else {
+                    u01 = f2_fma(f2(w4.x, w4.y), u01, f2(b4.x, b4.y));
+                    u23 = f2_fma(f2(w4.z, w4.w), u23, f2(b4.z, b4.w));
+                }
                 f2_split(u01, y0, y1);
                 f2_split(u23, y2, y3);
                 o[l][0] = pack_rn<T>(y0, y1);
@@ -181,7 +208,7 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
 // nothing), so every shuffle sees the full warp.
 // ---------------------------------------------------------------------
 
-template <DT T>
+template <DT T, bool RMS>
 __global__ void __launch_bounds__(kQkThreads)
 qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out,
                   const uint16_t *k, int64_t rows_k, const uint16_t *wq, const uint16_t *bq,
@@ -192,9 +219,9 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
     pdl_trigger();
     for (int c = threadIdx.x; c < 128; c += kQkThreads) {
         aff[0][0][c] = rows_q ? h_f32<T>(wq[c]) : 0.0f;
-        aff[0][1][c] = rows_q ? h_f32<T>(bq[c]) : 0.0f;
+        aff[0][1][c] = (!RMS && rows_q) ? h_f32<T>(bq[c]) : 0.0f;
         aff[1][0][c] = rows_k ? h_f32<T>(wk[c]) : 0.0f;
-        aff[1][1][c] = rows_k ? h_f32<T>(bk[c]) : 0.0f;
+        aff[1][1][c] = (!RMS && rows_k) ? h_f32<T>(bk[c]) : 0.0f;
     }
     __syncthreads();
 
@@ -226,11 +253,18 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
         }
 
         // Welford of lane pair (4k + 2t, 4k + 2t + 1), one f32x2 chain per k
+        // (RMS: the sums of squares in qq)
         f2_t m[8], qq[8];
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t *a0 = v[kk], *a1 = v[kk] + 2;
             m[kk] = qq[kk] = f2(0.f, 0.f);
+            if constexpr (RMS) {
+                const f2_t e0 = f2(lo_f32<T>(a0[0]), lo_f32<T>(a1[0])), e1 = f2(hi_f32<T>(a0[0]), hi_f32<T>(a1[0]));
+                const f2_t e2 = f2(lo_f32<T>(a0[1]), lo_f32<T>(a1[1])), e3 = f2(hi_f32<T>(a0[1]), hi_f32<T>(a1[1]));
+                qq[kk] = f2_add(f2_add(f2_add(f2_mul(e0, e0), f2_mul(e1, e1)), f2_mul(e2, e2)), f2_mul(e3, e3));
+                continue;
+            }
             push2(m[kk], qq[kk], f2(lo_f32<T>(a0[0]), lo_f32<T>(a1[0])), Rcp<1>::value);
             push2(m[kk], qq[kk], f2(hi_f32<T>(a0[0]), hi_f32<T>(a1[0])), Rcp<2>::value);
             push2(m[kk], qq[kk], f2(lo_f32<T>(a0[1]), lo_f32<T>(a1[1])), Rcp<3>::value);
@@ -244,34 +278,50 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
             const int64_t ks = nb > rows_q ? nb : rows_q;
             if (ne > ks) prefetch_l2(k + (ks - rows_q) * 128, (uint64_t)(ne - ks) * 256);
         }
-        // offsets 16, 8, 4: k with k + 4, k + 2, k + 1 (all lane counts equal)
+        float mean, rstd;
+        if constexpr (RMS) {
+            // offsets 16, 8, 4 inside the thread, 2 across the thread pair, 1 on the halves
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            chan_p2(m[kk], qq[kk], m[kk + 4], qq[kk + 4], f2(qk_coef(0, 16, NL), qk_coef(0, 16, NL)),
-                    f2(qk_count(0, 16, NL), qk_count(0, 16, NL)));
+            for (int kk = 0; kk < 4; ++kk) qq[kk] = f2_add(qq[kk], qq[kk + 4]);
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-            chan_p2(m[kk], qq[kk], m[kk + 2], qq[kk + 2], f2(qk_coef(0, 8, NL), qk_coef(0, 8, NL)),
-                    f2(qk_count(0, 8, NL), qk_count(0, 8, NL)));
-        chan_p2(m[0], qq[0], m[1], qq[1], f2(qk_coef(0, 4, NL), qk_coef(0, 4, NL)),
-                f2(qk_count(0, 4, NL), qk_count(0, 4, NL)));
-        {  // offset 2: the partner thread holds lanes with the other t
-            const f2_t pm = __shfl_xor_sync(0xffffffffu, m[0], 1);
-            const f2_t pq = __shfl_xor_sync(0xffffffffu, qq[0], 1);
-            const f2_t lo = t ? pm : m[0], up = t ? m[0] : pm;
-            const f2_t delta = f2_sub(up, lo);
-            const f2_t c2 = f2(qk_coef(0, 2, NL), qk_coef(0, 2, NL));
-            m[0] = f2_fma(delta, c2, lo);
-            qq[0] = f2_fma(f2_mul(f2_mul(delta, delta), f2(qk_count(0, 2, NL), qk_count(0, 2, NL))), c2,
-                           f2_add(qq[0], pq));
+            for (int kk = 0; kk < 2; ++kk) qq[kk] = f2_add(qq[kk], qq[kk + 2]);
+            qq[0] = f2_add(qq[0], qq[1]);
+            qq[0] = f2_add(qq[0], __shfl_xor_sync(0xffffffffu, qq[0], 1));
+            float a0, a1;
+            f2_split(qq[0], a0, a1);
+            mean = 0.0f;
+            rstd = rsqrt_rn(__fadd_rn(__fdiv_rn(__fadd_rn(a0, a1), 128.0f), eps));
+        } else {
+            // offsets 16, 8, 4: k with k + 4, k + 2, k + 1 (all lane counts equal)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                chan_p2(m[kk], qq[kk], m[kk + 4], qq[kk + 4], f2(qk_coef(0, 16, NL), qk_coef(0, 16, NL)),
+                        f2(qk_count(0, 16, NL), qk_count(0, 16, NL)));
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+                chan_p2(m[kk], qq[kk], m[kk + 2], qq[kk + 2], f2(qk_coef(0, 8, NL), qk_coef(0, 8, NL)),
+                        f2(qk_count(0, 8, NL), qk_count(0, 8, NL)));
+            chan_p2(m[0], qq[0], m[1], qq[1], f2(qk_coef(0, 4, NL), qk_coef(0, 4, NL)),
+                    f2(qk_count(0, 4, NL), qk_count(0, 4, NL)));
+            {  // offset 2: the partner thread holds lanes with the other t
+                const f2_t pm = __shfl_xor_sync(0xffffffffu, m[0], 1);
+                const f2_t pq = __shfl_xor_sync(0xffffffffu, qq[0], 1);
+                const f2_t lo = t ? pm : m[0], up = t ? m[0] : pm;
+                const f2_t delta = f2_sub(up, lo);
+                const f2_t c2 = f2(qk_coef(0, 2, NL), qk_coef(0, 2, NL));
+                m[0] = f2_fma(delta, c2, lo);
+                qq[0] = f2_fma(f2_mul(f2_mul(delta, delta), f2(qk_count(0, 2, NL), qk_count(0, 2, NL))), c2,
+                               f2_add(qq[0], pq));
+            }
+            float a0, a1, b0, b1;
+            f2_split(m[0], a0, a1);
+            f2_split(qq[0], b0, b1);
+            chan_p(a0, b0, a1, b1, qk_coef(0, 1, NL), qk_count(0, 1, NL));  // offset 1
+            mean = a0;
+            rstd = rsqrt_rn(__fadd_rn(__fdiv_rn(b0, 128.0f), eps));
         }
-        float a0, a1, b0, b1;
-        f2_split(m[0], a0, a1);
-        f2_split(qq[0], b0, b1);
-        chan_p(a0, b0, a1, b1, qk_coef(0, 1, NL), qk_count(0, 1, NL));  // offset 1
-        const float rstd = rsqrt_rn(__fadd_rn(__fdiv_rn(b0, 128.0f), eps));
 
-        const f2_t mm = f2(a0, a0), rr = f2(rstd, rstd);
+        const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             uint32_t o[4];
@@ -285,8 +335,13 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
                 unpack_again<T>(v[kk][2 * h + 1], x2, x3);
                 f2_t u01 = f2_mul(f2_sub(f2(x0, x1), mm), rr);
                 f2_t u23 = f2_mul(f2_sub(f2(x2, x3), mm), rr);
-                u01 = f2_fma(f2(w4.x, w4.y), u01, f2(b4.x, b4.y));
-                u23 = f2_fma(f2(w4.z, w4.w), u23, f2(b4.z, b4.w));
+                if constexpr (RMS) {
+                    u01 = f2_mul(f2(w4.x, w4.y), u01);
+                    u23 = f2_mul(f2(w4.z, w4.w), u23);
+                } else {
+                    u01 = f2_fma(f2(w4.x, w4.y), u01, f2(b4.x, b4.y));
+                    u23 = f2_fma(f2(w4.z, w4.w), u23, f2(b4.z, b4.w));
+                }
                 f2_split(u01, y0, y1);
                 f2_split(u23, y2, y3);
                 o[2 * h] = pack_rn<T>(y0, y1);
@@ -297,9 +352,9 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
     }
 }
 
-template <DT T>
+template <DT T, bool RMS>
 static cudaError_t run_qk_pair(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    auto kern = qk_ln_pair_kernel<T>;
+    auto kern = qk_ln_pair_kernel<T, RMS>;
     const int64_t total = a.rows_q + a.rows_k;
     const int64_t ctas = (total * 2 + kQkThreads - 1) / kQkThreads;
     const int64_t grid = imin64(ctas, (int64_t)dev.sms * blocks_per_sm(kern, kQkThreads, 0));
@@ -309,9 +364,9 @@ static cudaError_t run_qk_pair(const QkArgs &a, bool pdl, cudaStream_t s, const 
                     (const uint16_t *)a.bk, a.eps);
 }
 
-template <DT T, int NL>
+template <DT T, int NL, bool RMS>
 static cudaError_t run_qk(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    auto kern = qk_ln_kernel<T, NL>;
+    auto kern = qk_ln_kernel<T, NL, RMS>;
     const int64_t total = a.rows_q + a.rows_k;
     const int64_t ctas = (total + kQkThreads - 1) / kQkThreads;
     const int64_t grid = imin64(ctas, (int64_t)dev.sms * blocks_per_sm(kern, kQkThreads, 0));
@@ -323,17 +378,19 @@ static cudaError_t run_qk(const QkArgs &a, bool pdl, cudaStream_t s, const Devic
 
 static bool al(const void *p, int a) { return p == nullptr || ((uintptr_t)p % (uintptr_t)a) == 0; }
 
-template <DT T>
+template <DT T, bool RMS>
 static cudaError_t qk_dispatch(const QkArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     const bool a16 = al(a.q, 16) && al(a.k, 16) && al(a.q_out, 16) && al(a.k_out, 16);
-    if (a.Dh == 128) return a16 ? run_qk_pair<T>(a, pdl, s, dev) : run_qk<T, 32>(a, pdl, s, dev);
-    if (a.Dh == 64) return run_qk<T, 16>(a, pdl, s, dev);
-    return run_qk<T, 0>(a, pdl, s, dev);
+    if (a.Dh == 128) return a16 ? run_qk_pair<T, RMS>(a, pdl, s, dev) : run_qk<T, 32, RMS>(a, pdl, s, dev);
+    if (a.Dh == 64) return run_qk<T, 16, RMS>(a, pdl, s, dev);
+    return run_qk<T, 0, RMS>(a, pdl, s, dev);
 }
 
+// LayerNorm with affine, or (a.rms) RMSNorm with a weight
 cudaError_t launch_qk_head_layernorm(const QkArgs &a, int dtype, bool pdl, cudaStream_t s,
                                      const DeviceInfo &dev) {
-    return dtype == 0 ? qk_dispatch<DT::BF16>(a, pdl, s, dev) : qk_dispatch<DT::FP16>(a, pdl, s, dev);
+    if (a.rms) return dtype == 0 ? qk_dispatch<DT::BF16, true>(a, pdl, s, dev) : qk_dispatch<DT::FP16, true>(a, pdl, s, dev);
+    return dtype == 0 ? qk_dispatch<DT::BF16, false>(a, pdl, s, dev) : qk_dispatch<DT::FP16, false>(a, pdl, s, dev);
 }
 
 }  // namespace adaln

@@ -2,13 +2,18 @@
  * adaln.h -- C ABI of the fused non-GEMM chains of a diffusion-transformer
  * block, for NVIDIA GB300 (sm_103a).
  *
- * Four operations, each the fused form of an eager PyTorch chain described
- * on the SGLang Diffusion "Fused Kernels" page and its pull-request pages:
+ * The fused forms of eager PyTorch chains described on the SGLang Diffusion
+ * "Fused Kernels" page and its pull-request pages:
  *
  *   adaln_ln_modulate          LayerNorm (no affine) + adaLN modulate
  *   adaln_qk_head_layernorm    per-head LayerNorm with affine on q and k
  *   adaln_residual_gate_add    x + gate * y
  *   adaln_bias_gelu_tanh       tanh-GELU of (x + bias)
+ *   adaln_residual_gate_ln_modulate   x + gate * y, then LayerNorm + modulate
+ *   adaln_norm_scale_shift     LayerNorm or RMSNorm + modulate, optional
+ *                              residual gate, per-sample or per-token rows
+ *   adaln_rmsnorm_scale_shift  RMSNorm (no affine) + modulate
+ *   adaln_qk_rmsnorm           per-head RMSNorm with a weight on q and k
  *
  * Conventions shared by every call
  * --------------------------------
@@ -57,6 +62,10 @@ typedef enum adaln_dtype {
     ADALN_BF16 = 0,
     ADALN_FP16 = 1
 } adaln_dtype;
+
+/* norm kinds of adaln_norm_scale_shift */
+#define ADALN_NORM_LAYER 0 /* LayerNorm without affine */
+#define ADALN_NORM_RMS 1   /* RMSNorm without affine */
 
 /* flags */
 #define ADALN_FLAG_PDL 1u /* launch with programmatic dependent launch: the
@@ -182,6 +191,30 @@ adaln_status adaln_can_qk_head_layernorm(const void *q_out, const void *q, int64
                                          float eps, int dtype, uint32_t flags);
 
 /* ------------------------------------------------------------------------
+ * adaln_qk_rmsnorm
+ *   q_out[r, :] = RMSNorm(q[r, :]) * wq,  k_out[r, :] = RMSNorm(k[r, :]) * wk
+ *
+ * The per-head QK RMSNorm of the Fused Kernels page (Normalization table:
+ * qk_rmsnorm_native), q and k in one launch.  Shapes, layouts, limits,
+ * aliasing and statuses as adaln_qk_head_layernorm without the biases
+ * (rows of Dh contiguous values, 4 <= Dh <= 128, Dh % 4 == 0, 8-byte
+ * aligned tensors; rows_q or rows_k may be 0 with its pointers NULL).
+ * Numerics: 32 logical lanes, lane l holds elements 4l..4l+3 and sums
+ * round(v * v) serially; lanes added in the butterfly order 16, 8, 4, 2, 1;
+ * rstd = correctly rounded 1/sqrt(ss / Dh + eps); out = round(w * u) with
+ * u = round(rstd * x), both products in binary32.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_qk_rmsnorm(void *q_out, const void *q, int64_t rows_q,
+                              void *k_out, const void *k, int64_t rows_k, int64_t Dh,
+                              const void *wq, const void *wk,
+                              float eps, int dtype, uint32_t flags, void *stream);
+
+adaln_status adaln_can_qk_rmsnorm(const void *q_out, const void *q, int64_t rows_q,
+                                  const void *k_out, const void *k, int64_t rows_k,
+                                  int64_t Dh, const void *wq, const void *wk,
+                                  float eps, int dtype, uint32_t flags);
+
+/* ------------------------------------------------------------------------
  * adaln_residual_gate_add
  *   out[b, n, d] = x[b, n, d] + gate[b, d] * y[b, n, d]
  *
@@ -219,10 +252,11 @@ adaln_status adaln_can_residual_gate_add(const void *out, const void *x, const v
  *   r_out may equal x or y (an in-place residual update); out overlaps none
  *   of the others.
  *   Limits: those of adaln_residual_gate_add and adaln_ln_modulate (D % 4
- *   == 0, eps finite and >= 0).  One kernel when D <= 4096, the rows are
- *   8-byte aligned and the gate rows are 8-byte aligned with s_gate_b % 4
- *   == 0; otherwise the gate-add kernel writes r_out and the LN+modulate
- *   kernel reads it back (two launches on the stream, same bits).
+ *   == 0, eps finite and >= 0).  One launch: the contiguous-rows kernel when
+ *   D <= 4096, the rows are 8-byte aligned and the gate rows are 8-byte
+ *   aligned with s_gate_b % 4 == 0; otherwise the general kernel (same
+ *   bits).  This is adaln_norm_scale_shift with ADALN_NORM_LAYER, one gate,
+ *   scale and shift row per sample.
  * Numerics: r_out = round(x + round(gate * y)); out is adaln_ln_modulate of
  * r_out as stored (bit for bit the two calls in sequence).
  * Returns the statuses of the two calls it combines; ADALN_E_OVERLAP also
@@ -236,6 +270,100 @@ adaln_status adaln_residual_gate_ln_modulate(void *r_out, void *out, const void 
                                              const void *shift, int64_t s_shift_b,
                                              float eps, int dtype, uint32_t flags,
                                              void *stream);
+
+/* ------------------------------------------------------------------------
+ * adaln_norm_scale_shift
+ *   v[b, n, :]     = x[b, n, :]                                  (gate NULL)
+ *   v[b, n, :]     = x[b, n, :] + gate[b, n, :] * y[b, n, :]     (otherwise;
+ *                                                   stored to r_out)
+ *   out[b, n, :]   = norm(v[b, n, :]) * (1 + scale[b, n, :]) + shift[b, n, :]
+ *
+ * The norm + scale/shift chains of the Fused Kernels page (Normalization
+ * table: layernorm_modulate, rmsnorm_scale_shift and, with a gate,
+ * scale_residual_norm_scale_shift) with the broadcast modes of its
+ * request-gated fusion table: per-token [B, S, 1] gates and per-token
+ * modulation rows read through strided [B, S, 6D] chunk views.
+ *   norm   ADALN_NORM_LAYER (affine-free LayerNorm, the statistics of
+ *          adaln_ln_modulate) or ADALN_NORM_RMS (affine-free RMSNorm).
+ *   x      (B, N, D), element (b, n, d) at x[b*sxB + n*sxN + d*sxD]; with a
+ *          gate x must be contiguous (sxD == 1, sxN == D, sxB == N*D).
+ *   gate   NULL, or element (b, n, d) at gate[b*s_gate_b + n*s_gate_n +
+ *          d*s_gate_d] with s_gate_d 1 (a row) or 0 (one value per token,
+ *          a [B, S, 1] gate); s_gate_n == 0 broadcasts one row per sample.
+ *   y, r_out  with a gate: (B, N, D) contiguous; r_out may equal x or y (an
+ *          in-place residual update), out overlaps none of x, y, r_out and
+ *          the gate.  Ignored (may be NULL) without a gate.
+ *   scale, shift  element (b, n, d) at scale[b*s_scale_b + n*s_scale_n + d]
+ *          (contiguous over d): s_scale_n == 0 gives the per-sample (B, 1, D)
+ *          rows; the chunk c of a per-token (B, N, nmod*D) table is
+ *          (table + c*D, N*nmod*D, nmod*D).
+ *   out    (B, N, D) contiguous; may equal x only without a gate and when x
+ *          is contiguous.  r_out and out overlap no scale / shift element.
+ *   Limits: B, N >= 1; 4 <= D <= 65536, D % 4 == 0; eps finite and >= 0.
+ *   Kernels: the contiguous-rows kernel when x is contiguous over d,
+ *   D <= 4096 and the rows (and strides) keep 8-byte alignment; the
+ *   transposed-view tile kernels for the LayerNorm with per-sample rows and
+ *   no gate; otherwise a general kernel.  Every kernel gives the same bits.
+ * Numerics: with a gate v = round(x + round(gate * y)) as stored in r_out.
+ *   LayerNorm: the Welford / Chan DAG of adaln_ln_modulate.  RMSNorm: the
+ *   same 128 logical lanes and chunk order, each lane accumulating
+ *   s = round(s + round(v * v)), lanes added in the butterfly order 16, 8,
+ *   4, 2, 1, 64, 32, ms = s / D, rstd = correctly rounded 1/sqrt(ms + eps),
+ *   mean taken as 0.  Then per element y = round(rstd * (v - mean)),
+ *   op = round(1 + scale), p = round(y * op), out = round(p + shift).
+ * Returns ADALN_E_VALUE for an unknown norm, ADALN_E_NULL for a gate
+ * without y or r_out, ADALN_E_STRIDE for a gate with non-contiguous x or
+ * s_gate_d other than 0 / 1, and the statuses of adaln_ln_modulate.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_norm_scale_shift(int norm, void *r_out, void *out, const void *x,
+                                    int64_t B, int64_t N, int64_t D,
+                                    int64_t sxB, int64_t sxN, int64_t sxD,
+                                    const void *gate, int64_t s_gate_b, int64_t s_gate_n,
+                                    int64_t s_gate_d, const void *y,
+                                    const void *scale, int64_t s_scale_b, int64_t s_scale_n,
+                                    const void *shift, int64_t s_shift_b, int64_t s_shift_n,
+                                    float eps, int dtype, uint32_t flags, void *stream);
+
+adaln_status adaln_can_norm_scale_shift(int norm, const void *r_out, const void *out,
+                                        const void *x, int64_t B, int64_t N, int64_t D,
+                                        int64_t sxB, int64_t sxN, int64_t sxD,
+                                        const void *gate, int64_t s_gate_b, int64_t s_gate_n,
+                                        int64_t s_gate_d, const void *y,
+                                        const void *scale, int64_t s_scale_b, int64_t s_scale_n,
+                                        const void *shift, int64_t s_shift_b, int64_t s_shift_n,
+                                        float eps, int dtype, uint32_t flags);
+
+/* Which kernel adaln_norm_scale_shift would launch, with the codes of
+ * adaln_ln_modulate_variant, or -status when the arguments are invalid. */
+int adaln_norm_scale_shift_variant(int norm, const void *r_out, const void *out,
+                                   const void *x, int64_t B, int64_t N, int64_t D,
+                                   int64_t sxB, int64_t sxN, int64_t sxD,
+                                   const void *gate, int64_t s_gate_b, int64_t s_gate_n,
+                                   int64_t s_gate_d, const void *y,
+                                   const void *scale, int64_t s_scale_b, int64_t s_scale_n,
+                                   const void *shift, int64_t s_shift_b, int64_t s_shift_n,
+                                   float eps, int dtype, uint32_t flags);
+
+/* ------------------------------------------------------------------------
+ * adaln_rmsnorm_scale_shift
+ *   out[b, n, :] = RMSNorm(x[b, n, :]) * (1 + scale[b, n, :]) + shift[b, n, :]
+ *
+ * The "rmsnorm_scale_shift" of the Fused Kernels page (Normalization table:
+ * RMSNorm + `* (1 + scale) + shift`, bit-exact, replacing four kernels):
+ * adaln_norm_scale_shift with ADALN_NORM_RMS and no gate; same arguments,
+ * limits, numerics and statuses.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_rmsnorm_scale_shift(void *out, const void *x, int64_t B, int64_t N, int64_t D,
+                                       int64_t sxB, int64_t sxN, int64_t sxD,
+                                       const void *scale, int64_t s_scale_b, int64_t s_scale_n,
+                                       const void *shift, int64_t s_shift_b, int64_t s_shift_n,
+                                       float eps, int dtype, uint32_t flags, void *stream);
+
+adaln_status adaln_can_rmsnorm_scale_shift(const void *out, const void *x, int64_t B, int64_t N,
+                                           int64_t D, int64_t sxB, int64_t sxN, int64_t sxD,
+                                           const void *scale, int64_t s_scale_b, int64_t s_scale_n,
+                                           const void *shift, int64_t s_shift_b, int64_t s_shift_n,
+                                           float eps, int dtype, uint32_t flags);
 
 adaln_status adaln_can_residual_gate_ln_modulate(const void *r_out, const void *out,
                                                  const void *x, const void *gate,

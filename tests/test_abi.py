@@ -138,3 +138,48 @@ def test_residual_ln_validation(ad):
     assert f(*args(fl=4)) == 6
     assert f(*args(g=0)) == 1
     assert f(*args(x=X + 1)) == 4               # odd address
+
+
+def test_norm_scale_shift_validation(ad):
+    f = ad.capi.adaln_can_norm_scale_shift
+    R, O, Y = 1 << 36, 1 << 37, 1 << 38
+    T = 1 << 39                                  # a per-token (B, N, 6, D) table
+    B, N, D = 2, 64, 1024
+
+    def args(norm=1, r=R, o=O, x=X, g=T, sgb=N * 6 * D, sgn=6 * D, sgd=1, y=Y, sc=T + 2 * D, ssn=6 * D,
+             sh=T + 4 * D, eps=1e-6, dt=0, fl=0, strides=None):
+        return (norm, r, o, x, B, N, D, *(strides or (N * D, D, 1)), g, sgb, sgn, sgd, y, sc, N * 6 * D, ssn,
+                sh, N * 6 * D, ssn, eps, dt, fl)
+
+    assert f(*args()) == 0
+    assert f(*args(norm=0)) == 0
+    assert f(*args(norm=2)) == 6                 # unknown norm
+    assert f(*args(sgd=0, sgn=1, sgb=N, g=T)) == 0   # a per-token scalar gate
+    assert f(*args(sgd=2)) == 5                  # gate element stride must be 0 or 1
+    assert f(*args(y=0)) == 1 and f(*args(r=0)) == 1
+    assert f(*args(strides=(N * D * 2, D * 2, 2))) == 5   # a gate needs contiguous x
+    assert f(*args(r=X)) == 0 and f(*args(r=Y)) == 0      # in-place residual update
+    assert f(*args(o=X)) == 7 and f(*args(o=R)) == 7
+    assert f(*args(r=T + 64)) == 7               # r into the table
+    assert f(*args(o=T + 2 * D + 6 * D * N + 8)) == 7     # out into a later token's scale row
+    assert f(*args(ssn=-6 * D)) == 5
+    # without a gate: any strides, y / r ignored, out == contiguous x allowed
+    assert f(*args(g=0, y=0, r=0)) == 0
+    assert f(*args(g=0, y=0, r=0, o=X)) == 0
+    assert f(*args(g=0, y=0, r=0, strides=(N * D * 2, 1, N * 2))) == 0
+    g = ad.capi.adaln_can_rmsnorm_scale_shift
+    assert g(O, X, B, N, D, N * D, D, 1, T, 0, 0, T + 2 * D, 0, 0, 1e-6, 0, 0) == 0
+    assert g(O, X, B, N, D, N * D, D, 1, T, 0, 0, T + 2 * D, 0, 0, float("nan"), 0, 0) == 6
+    assert g(T + 2 * D, X, B, N, D, N * D, D, 1, T, 0, 0, T + 2 * D, 0, 0, 1e-6, 0, 0) == 7
+
+
+def test_qk_rmsnorm_validation(ad):
+    f = ad.capi.adaln_can_qk_rmsnorm
+    Q, K, QO, KO, W = 1 << 36, 1 << 37, 1 << 38, 1 << 39, 1 << 40
+    assert f(QO, Q, 100, KO, K, 100, 128, W, W + 256, 1e-6, 0, 0) == 0
+    assert f(QO, Q, 100, None, None, 0, 128, W, None, 1e-6, 0, 0) == 0
+    assert f(QO, Q, 100, KO, K, 100, 130, W, W + 256, 1e-6, 0, 0) == 3
+    assert f(QO, Q, 100, KO, K, 100, 128, None, W, 1e-6, 0, 0) == 1
+    assert f(QO, Q, 100, KO, K, 100, 128, W, W + 256, 1e-6, 0, 0) == 0
+    assert f(W, Q, 100, KO, K, 100, 128, W, W + 256, 1e-6, 0, 0) == 7   # q_out on the weight
+    assert f(QO, Q, 100, KO, K, 100, 128, W + 4, W + 256, 1e-6, 0, 0) == 4
