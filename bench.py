@@ -243,6 +243,39 @@ def make_workloads(dev, which, n_sets=None, flags=0):
         out["qk"] = ([(lambda t=t: ad.qk_head_layernorm(t[0], t[1], t[2], t[3], t[4], t[5], 1e-6, q_out=t[6],
                                                        k_out=t[7], flags=flags))
                       for t in copies(base, sets_for(nb))], nb, w.name)
+    if "rms" in which:
+        w = synth.rms_rows()
+        nb = ln_bytes(1, 4096, 4096)
+        base = [torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift")]
+        base.append(torch.empty_like(base[0]))
+        out["rms"] = ([(lambda x=x, sc=sc, sh=sh, o=o: ad.rmsnorm_scale_shift(x, sc, sh, 1e-6, out=o, flags=flags))
+                       for x, sc, sh, o in copies(base, sets_for(nb))], nb, w.name)
+    if "rms_tok" in which:
+        w = synth.rms_tokens()
+        nb = 4 * 4096 * 4096 * 2  # x, the scale and shift rows of every token, out
+        base = [torch_bits(w.tensors["x"].draw(), "bf16", dev), torch_bits(w.tensors["table"].draw(), "bf16", dev)]
+        base.append(torch.empty_like(base[0]))
+        out["rms_tok"] = ([(lambda x=x, t=t, o=o: ad.rmsnorm_scale_shift(x, t[:, :, 1], t[:, :, 0], 1e-6, out=o,
+                                                                          flags=flags))
+                           for x, t, o in copies(base, sets_for(nb))], nb, w.name)
+    if "gate_rms_tok" in which:
+        w = synth.gate_rms_tokens()
+        nb = 6 * 4096 * 4096 * 2 + 4096 * 2  # x, y, scale, shift rows read; r, out written; the gates
+        base = [torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "y", "gate", "table")]
+        base += [torch.empty_like(base[0]), torch.empty_like(base[0])]
+        out["gate_rms_tok"] = ([(lambda t=t: ad.norm_scale_shift(t[0], t[3][:, :, 1], t[3][:, :, 0], 1e-6, norm="rms",
+                                                                 gate=t[2], y=t[1], r_out=t[4], out=t[5],
+                                                                 flags=flags))
+                                for t in copies(base, sets_for(nb))], nb, w.name)
+    if "qk_rms" in which:
+        w = synth.qk_rms()
+        rows = 4096 * 30
+        nb = 2 * 2 * rows * 128 * 2 + 2 * 128 * 2
+        base = [torch_bits(w.tensors[n].draw(), "bf16", dev) for n in ("q", "k", "wq", "wk")]
+        base += [torch.empty_like(base[0]), torch.empty_like(base[1])]
+        out["qk_rms"] = ([(lambda t=t: ad.qk_rmsnorm(t[0], t[1], t[2], t[3], 1e-6, q_out=t[4], k_out=t[5],
+                                                    flags=flags))
+                          for t in copies(base, sets_for(nb))], nb, w.name)
     for dt in ("bf16", "fp16"):
         key = f"gelu_{dt}"
         if key in which:
@@ -289,6 +322,21 @@ def make_eager(dev, name, nb):
             w = [g((128,), 0.05) for _ in range(4)]
             out.append(lambda q=q, k=k, w=w: (F.layer_norm(q, (128,), w[0], w[1], 1e-6),
                                               F.layer_norm(k, (128,), w[2], w[3], 1e-6)))
+        elif name == "rms":
+            x, sc, sh = g((1, 4096, 4096)), g((1, 1, 4096), 0.1), g((1, 1, 4096), 0.1)
+            out.append(lambda x=x, sc=sc, sh=sh: F.rms_norm(x, (4096,), eps=1e-6) * (1 + sc) + sh)
+        elif name == "rms_tok":
+            x, t = g((1, 4096, 4096)), g((1, 4096, 6, 4096), 0.1)
+            out.append(lambda x=x, t=t: F.rms_norm(x, (4096,), eps=1e-6) * (1 + t[:, :, 1]) + t[:, :, 0])
+        elif name == "gate_rms_tok":
+            x, y, gt, t = g((1, 4096, 4096)), g((1, 4096, 4096)), g((1, 4096, 1), 0.5), g((1, 4096, 6, 4096), 0.1)
+            out.append(lambda x=x, y=y, gt=gt, t=t: (
+                lambda r: (r, F.rms_norm(r, (4096,), eps=1e-6) * (1 + t[:, :, 1]) + t[:, :, 0]))(x + gt * y))
+        elif name == "qk_rms":
+            q, k = g((1, 4096, 30, 128), 2.0), g((1, 4096, 30, 128), 2.0)
+            wq, wk = g((128,), 0.05), g((128,), 0.05)
+            out.append(lambda q=q, k=k, wq=wq, wk=wk: (F.rms_norm(q, (128,), wq, 1e-6),
+                                                       F.rms_norm(k, (128,), wk, 1e-6)))
         elif name.startswith("gelu_"):
             dt = torch.bfloat16 if name == "gelu_bf16" else torch.float16
             x, b = g((32760, 13824)).to(dt), g((13824,), 0.02).to(dt)
@@ -651,7 +699,7 @@ def run_ours(args):
                        "one_stream_ms_per_step": round(serial_ms, 4)}
     if rank == 0 and not args.no_per_config:
         names = ["tiny", "sana", "sana_nmod2", "glm_ln", "glm_gate", "glm_gate_ln", "qk", "gelu_bf16",
-                 "gelu_fp16"]
+                 "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms"]
         per = {}
         steps = max(20, min(args.steps, 400))
         for name in names:
@@ -702,7 +750,7 @@ def main():
     p.add_argument("--quick", action="store_true", help="headline only (for profiler runs)")
     p.add_argument("--only", default="sana",
                    choices=["sana", "sana_nmod2", "tiny", "glm_ln", "glm_gate", "glm_gate_ln", "qk",
-                            "gelu_bf16", "gelu_fp16"],
+                            "gelu_bf16", "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms"],
                    help="workload timed as the headline (profiling runs); the JSON line's metric "
                         "and roofline describe the Sana LN+modulate only when this is 'sana'")
     args = p.parse_args()

@@ -155,6 +155,48 @@ def gelu_wan(dtype: str = "bf16") -> Workload:
     }, {"dtype": dtype})
 
 
+def rms_rows(N: int = 4096, D: int = 4096) -> Workload:
+    """RMSNorm + modulate with one scale / shift row per sample, the GLM
+    LayerNorm's shape."""
+    return Workload(f"rmsnorm_scale_shift (1,{N},{D}) per-sample rows", "rmsnorm_scale_shift", {
+        "x": TensorSpec((1, N, D), 0.0, 1.0, SEEDS["x"]),
+        "scale": TensorSpec((1, 1, D), 0.0, 0.1, SEEDS["scale"]),
+        "shift": TensorSpec((1, 1, D), 0.0, 0.1, SEEDS["shift"]),
+    }, {"eps": 1e-6})
+
+
+def rms_tokens(N: int = 4096, D: int = 4096) -> Workload:
+    """RMSNorm + modulate with per-token scale / shift: chunks 1 and 0 of a
+    (1, N, 6, D) modulation table (the strided [B, S, 6D] chunk views)."""
+    return Workload(f"rmsnorm_scale_shift (1,{N},{D}) per-token rows of a (1,{N},6,{D}) table",
+                    "rmsnorm_scale_shift", {
+                        "x": TensorSpec((1, N, D), 0.0, 1.0, SEEDS["x"]),
+                        "table": TensorSpec((1, N, 6, D), 0.0, 0.1, SEEDS["table"]),
+                    }, {"eps": 1e-6})
+
+
+def gate_rms_tokens(N: int = 4096, D: int = 4096) -> Workload:
+    """r = x + gate * y with a per-token [1, N, 1] gate, then RMSNorm(r) *
+    (1 + scale) + shift with per-token rows of a (1, N, 6, D) table."""
+    return Workload(f"norm_scale_shift rms (1,{N},{D}) per-token gate [1,{N},1] and rows",
+                    "norm_scale_shift", {
+                        "x": TensorSpec((1, N, D), 0.0, 1.0, SEEDS["x"]),
+                        "y": TensorSpec((1, N, D), 0.0, 1.0, SEEDS["y"]),
+                        "gate": TensorSpec((1, N, 1), 0.0, 0.5, SEEDS["gate"]),
+                        "table": TensorSpec((1, N, 6, D), 0.0, 0.1, SEEDS["table"]),
+                    }, {"eps": 1e-6})
+
+
+def qk_rms(N: int = 4096, H: int = 30) -> Workload:
+    """Per-head QK RMSNorm with weights, H heads of 128 over N tokens."""
+    return Workload(f"qk_rmsnorm (1,{N},{H},128)", "qk_rmsnorm", {
+        "q": TensorSpec((1, N, H, 128), 0.0, 2.0, SEEDS["x"]),
+        "k": TensorSpec((1, N, H, 128), 0.0, 2.0, SEEDS["k"]),
+        "wq": TensorSpec((128,), 1.0, 0.05, SEEDS["wq"]),
+        "wk": TensorSpec((128,), 1.0, 0.05, SEEDS["wk"]),
+    }, {"eps": 1e-6})
+
+
 def all_workloads() -> List[Workload]:
     return [ln_tiny(), ln_sana(), ln_glm(), gate_add_glm(), qk_glm(), gelu_wan("bf16"),
-            gelu_wan("fp16")]
+            gelu_wan("fp16"), rms_rows(), rms_tokens(), gate_rms_tokens(), qk_rms()]
