@@ -20,6 +20,8 @@ Parity status of each function (what pins it, see ``tests/test_oracle_*``):
                      sign-flip and power-of-two symmetries; per-token rows
                      and gates equal per-row calls of the pinned forms
   qk_rmsnorm         pinned: fp64 RMSNorm with weight, exact rows
+  temb_table_slices  pinned: numpy's binary32 addition of the promoted
+                     operands, slice by slice
   bias_gelu_tanh     pinned: 100-bit evaluation of tanh-GELU on all inputs
   rsqrt_cr           pinned: 100-bit evaluation
 """
@@ -44,6 +46,7 @@ _lib = None
 _lock = threading.Lock()
 
 DTYPE_CODE = {"bf16": 0, "fp16": 1}
+ANY_DTYPE_CODE = {"bf16": 0, "fp16": 1, "fp32": 2}
 
 
 def build(force: bool = False) -> str:
@@ -81,6 +84,7 @@ def _lib_handle():
                 "oracle_norm_scale_shift": [_P, _P, _INT, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _I, _P,
                                             _P, _I, _I, _P, _I, _I, _F, _INT, _I, _I, _P, _P],
                 "oracle_qk_rmsnorm": [_P, _P, _I, _I, _P, _F, _INT, _I, _I],
+                "oracle_temb_table_slices": [_P, _I, _P, _INT, _P, _INT, _I, _I, _I, _I],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -372,6 +376,26 @@ def qk_rmsnorm(x: np.ndarray, Dh: int, w: np.ndarray, eps: float, dtype: str = "
 
     _run(_split_runs(runs, threads), one, threads)
     return idx, out
+
+
+def temb_table_slices(table: np.ndarray, table_dtype: str, temb: np.ndarray, temb_dtype: str,
+                      B: int, S: int, K: int, D: int) -> np.ndarray:
+    """``(table + temb.float()).chunk(K)`` as K contiguous binary32 slices
+    (Fused Kernels page, adaLN modulation and gating table: temb_table_slices).
+    table (K, D) and temb (B, S, K, D) hold uint16 patterns (bf16 / fp16) or
+    float32.  Returns a float32 array (K, B, S, D)."""
+    def arr(a, dt):
+        return np.ascontiguousarray(a, dtype=np.float32 if dt == "fp32" else np.uint16).reshape(-1)
+    t, e = arr(table, table_dtype), arr(temb, temb_dtype)
+    if t.size != K * D or e.size != B * S * K * D:
+        raise ValueError("table must hold K*D values and temb B*S*K*D")
+    out = np.zeros((K, B, S, D), dtype=np.float32)
+    rc = _lib_handle().oracle_temb_table_slices(out.ctypes.data, B * S * D, t.ctypes.data,
+                                                ANY_DTYPE_CODE[table_dtype], e.ctypes.data,
+                                                ANY_DTYPE_CODE[temb_dtype], B, S, K, D)
+    if rc:
+        raise ValueError("oracle_temb_table_slices rejected its arguments")
+    return out
 
 
 def bias_gelu_tanh(x: np.ndarray, bias: np.ndarray, rows_total: int, width: int,

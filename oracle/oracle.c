@@ -30,6 +30,9 @@
  *    and quality tiers" (the RMSNorm statistics are folded by a butterfly).
  *  - bias_gelu_tanh: PR #37075 "功能与动机" and "关键源码片段" (fp32 add,
  *    round to the storage type, then tanh-GELU, round again).
+ *  - temb_table_slices: "Fused Kernels", adaLN modulation and gating table
+ *    and its note on the op ((scale_shift_table + temb.float()).chunk(6)
+ *    into six contiguous slices in one pass).
  *
  * Readings where the pages leave a step open (each also listed in the design
  * notes): the reciprocal in the Welford push and every division are IEEE
@@ -476,6 +479,35 @@ int oracle_bias_gelu_tanh(uint16_t *out, const uint16_t *x, const uint16_t *bias
             uint16_t v = store16(load16(x[r * width + c], dtype) + load16(bias[c], dtype), dtype);
             out[(r - row_begin) * width + c] = tab[v];
         }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* temb_table_slices                                                    */
+/* ------------------------------------------------------------------ */
+
+/* Element of a 16-bit or binary32 array as binary32 (exact): dtype 0 bf16,
+ * 1 fp16, 2 binary32. */
+static float load_any(const void *p, int64_t i, int dtype) {
+    if (dtype == 2) return ((const float *)p)[i];
+    return load16(((const uint16_t *)p)[i], dtype);
+}
+
+/* out_k[b, s, d] = table[k, d] + temb[b, s, k, d] in binary32 (one IEEE
+ * addition of the exact binary32 values of both operands), for the K
+ * chunks of a (B, S, K, D) temb, each written to its own contiguous
+ * (B, S, D) slice at out + k * s_out_k.  table (K, D) and temb contiguous.
+ * Returns -1 for a bad dtype or size. */
+int oracle_temb_table_slices(float *out, int64_t s_out_k, const void *table, int table_dtype,
+                             const void *temb, int temb_dtype, int64_t B, int64_t S, int64_t K,
+                             int64_t D) {
+    if (table_dtype < 0 || table_dtype > 2 || temb_dtype < 0 || temb_dtype > 2) return -1;
+    if (B < 1 || S < 1 || K < 1 || D < 1) return -1;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t bs = 0; bs < B * S; ++bs)
+            for (int64_t d = 0; d < D; ++d)
+                out[k * s_out_k + bs * D + d] =
+                    load_any(table, k * D + d, table_dtype) + load_any(temb, (bs * K + k) * D + d, temb_dtype);
     return 0;
 }
 

@@ -24,6 +24,7 @@ import oracle
 import test_oracle_ln as ln
 import test_oracle_qk_gate_gelu as qg
 import test_oracle_rms as rm
+import test_oracle_temb as tb
 import test_oracle_rsqrt as rs
 import test_oracle_conversions as cv
 
@@ -65,6 +66,10 @@ MUTANTS = {
     "gated_norm_reads_x": ("for (int64_t d = 0; d < D; ++d) v[d] = gate_add(",
                            "for (int64_t d = 0; d < D && 0; ++d) v[d] = gate_add("),
     "qk_rms_weight_dropped": ("store16(load16(w[d], dtype) * u, dtype);", "store16(u, dtype);"),
+    "temb_chunk_major_layout": ("load_any(temb, (bs * K + k) * D + d, temb_dtype)",
+                                "load_any(temb, (k * B * S + bs) * D + d, temb_dtype)"),
+    "temb_table_row_zero": ("load_any(table, k * D + d, table_dtype)", "load_any(table, d, table_dtype)"),
+    "temb_slice_stride_ignored": ("out[k * s_out_k + bs * D + d] =", "out[k * B * S * D / K + bs * D + d] ="),
     "gelu_constant_typo": ("const long double k1 = 0.044715L;", "const long double k1 = 0.04715L;"),
     "gelu_sign": ("long double g = v / (1.0L + expl(-2.0L * z));", "long double g = v / (1.0L + expl(2.0L * z));"),
     "gelu_bias_dropped": ("uint16_t v = store16(load16(x[r * width + c], dtype) + load16(bias[c], dtype), dtype);",
@@ -122,6 +127,8 @@ def _pins():
         P.append((f"per_token_{norm}", lambda norm=norm: rm.test_per_token_rows_and_gates_equal_one_row_calls(None, norm)))
     P.append(("qk_rms", lambda: rm.test_qk_rms_within_rounding_bound(None, 128, "bf16")))
     P.append(("qk_rms_exact", lambda: rm.test_qk_rms_exact_rows(None, 64)))
+    P.append(("temb_add", lambda: tb.test_slices_equal_numpy_binary32_add(None, "fp32", "bf16")))
+    P.append(("temb_order", lambda: tb.test_slice_order_and_broadcast(None)))
     P.append(("bf16_encode", lambda: cv.test_bf16_encode_vs_torch(None)))
     P.append(("fp16_encode", lambda: cv.test_fp16_encode_vs_numpy(None)))
     return P
