@@ -10,7 +10,7 @@ Two layers:
     and so on), taking raw integers (device pointers, sizes, a stream handle);
   * ``ln_modulate``, ``qk_head_layernorm``, ``residual_gate_add``,
     ``bias_gelu_tanh``, ``residual_gate_ln_modulate``, ``norm_scale_shift``,
-    ``rmsnorm_scale_shift``, ``qk_rmsnorm``: the same calls taking torch
+    ``rmsnorm_scale_shift``, ``qk_rmsnorm``, ``temb_table_slices``: the same calls taking torch
     tensors (PyTorch only provides the device memory and the current stream).
 """
 from __future__ import annotations
@@ -73,6 +73,8 @@ _SIGS = {
     "adaln_can_rmsnorm_scale_shift": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _P, _I, _I, _F, _INT, _U], _INT),
     "adaln_qk_rmsnorm": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _F, _INT, _U, _P], _INT),
     "adaln_can_qk_rmsnorm": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _F, _INT, _U], _INT),
+    "adaln_temb_table_slices": ([_P, _I, _P, _INT, _P, _INT, _I, _I, _I, _I, _U, _P], _INT),
+    "adaln_can_temb_table_slices": ([_P, _I, _P, _INT, _P, _INT, _I, _I, _I, _I, _U], _INT),
 }
 
 
@@ -359,6 +361,34 @@ def qk_rmsnorm(q, k, wq, wk, eps: float, q_out=None, k_out=None, flags: int = 0,
                                _dtype_code(ref), flags, _stream(stream))
     _check(st, "adaln_qk_rmsnorm")
     return q_out, k_out
+
+
+def _any_dtype_code(t) -> int:
+    torch = _torch()
+    return 2 if t.dtype == torch.float32 else _dtype_code(t)
+
+
+def temb_table_slices(table, temb, out=None, flags: int = 0, stream=None):
+    """``(table + temb.float()).chunk(K, dim=2)`` as K contiguous float32
+    tensors (B, S, D), written in one pass.  table (K, D) or (1, K, D); temb
+    (B, S, K, D) or (B, K, D) (one row per sample), both contiguous, bf16,
+    fp16 or float32.  ``out`` may be a (K, B, S, D) float32 buffer.  Returns
+    the list of the K slices (views of one buffer)."""
+    torch = _torch()
+    if temb.dim() == 3:
+        temb = temb.unsqueeze(1)
+    B, S, K, D = temb.shape
+    table = table.reshape(-1, table.shape[-1])
+    if tuple(table.shape) != (K, D) or not table.is_contiguous() or not temb.is_contiguous():
+        raise ValueError("table (K, D) and temb (B, S, K, D) must be contiguous")
+    if out is None:
+        out = torch.empty((K, B, S, D), dtype=torch.float32, device=temb.device)
+    if tuple(out.shape) != (K, B, S, D) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 (K, B, S, D) buffer")
+    st = capi.adaln_temb_table_slices(out.data_ptr(), B * S * D, table.data_ptr(), _any_dtype_code(table),
+                                      temb.data_ptr(), _any_dtype_code(temb), B, S, K, D, flags, _stream(stream))
+    _check(st, "adaln_temb_table_slices")
+    return list(out.unbind(0))
 
 
 def bias_gelu_tanh(x, bias, out=None, flags: int = 0, stream=None):

@@ -251,6 +251,24 @@ LnArgs norm_args(int norm, void *r_out, void *out, const void *x, int64_t B, int
     return a;
 }
 
+adaln_status check_temb(const void *out, int64_t s_out_k, const void *table, int table_dtype, const void *temb,
+                        int temb_dtype, int64_t B, int64_t S, int64_t K, int64_t D, uint32_t flags) {
+    auto ok_dt = [](int d) { return d == ADALN_BF16 || d == ADALN_FP16 || d == ADALN_FP32; };
+    if (!ok_dt(table_dtype) || !ok_dt(temb_dtype)) return ADALN_E_DTYPE;
+    if (flags & ~ADALN_FLAG_PDL) return ADALN_E_VALUE;
+    if (!out || !table || !temb) return ADALN_E_NULL;
+    if (B < 1 || S < 1 || K < 1 || D < 1 || K > 65536 || D > 65536) return ADALN_E_SHAPE;
+    if (B > ((int64_t)1 << 40) / S || B * S > ((int64_t)1 << 44) / (K * D)) return ADALN_E_SHAPE;
+    const int64_t slice = B * S * D;
+    if (K > 1 && (s_out_k < slice || s_out_k > ((int64_t)1 << 46) / K)) return ADALN_E_STRIDE;
+    const int te = table_dtype == ADALN_FP32 ? 4 : 2, ee = temb_dtype == ADALN_FP32 ? 4 : 2;
+    if (((uintptr_t)out & 3u) || ((uintptr_t)table % te) || ((uintptr_t)temb % ee)) return ADALN_E_ALIGN;
+    const int64_t out_bytes = 4 * ((K - 1) * (K > 1 ? s_out_k : 0) + slice);
+    if (overlap(out, out_bytes, table, (int64_t)te * K * D) || overlap(out, out_bytes, temb, ee * slice * K))
+        return ADALN_E_OVERLAP;
+    return ADALN_OK;
+}
+
 adaln_status check_gelu(const void *out, const void *x, const void *bias, int64_t rows, int64_t width,
                         int dtype, uint32_t flags) {
     if (dtype != ADALN_BF16 && dtype != ADALN_FP16) return ADALN_E_DTYPE;
@@ -298,7 +316,7 @@ const char *adaln_status_str(int status) {
     switch (status) {
         case ADALN_OK: return "ADALN_OK";
         case ADALN_E_NULL: return "ADALN_E_NULL: a required pointer is NULL";
-        case ADALN_E_DTYPE: return "ADALN_E_DTYPE: dtype must be ADALN_BF16 or ADALN_FP16";
+        case ADALN_E_DTYPE: return "ADALN_E_DTYPE: dtype must be ADALN_BF16 or ADALN_FP16 (or ADALN_FP32 where allowed)";
         case ADALN_E_SHAPE: return "ADALN_E_SHAPE: a size is out of range";
         case ADALN_E_ALIGN: return "ADALN_E_ALIGN: a pointer is not aligned";
         case ADALN_E_STRIDE: return "ADALN_E_STRIDE: a stride is negative";
@@ -515,6 +533,24 @@ adaln_status adaln_qk_rmsnorm(void *q_out, const void *q, int64_t rows_q, void *
     QkArgs a{q_out, q, rows_q, k_out, k, rows_k, Dh, wq, nullptr, wk, nullptr, eps, true};
     return finish_launch(
         launch_qk_head_layernorm(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+adaln_status adaln_can_temb_table_slices(const void *out, int64_t s_out_k, const void *table, int table_dtype,
+                                        const void *temb, int temb_dtype, int64_t B, int64_t S, int64_t K,
+                                        int64_t D, uint32_t flags) {
+    return check_temb(out, s_out_k, table, table_dtype, temb, temb_dtype, B, S, K, D, flags);
+}
+
+adaln_status adaln_temb_table_slices(void *out, int64_t s_out_k, const void *table, int table_dtype,
+                                    const void *temb, int temb_dtype, int64_t B, int64_t S, int64_t K, int64_t D,
+                                    uint32_t flags, void *stream) {
+    adaln_status st = check_temb(out, s_out_k, table, table_dtype, temb, temb_dtype, B, S, K, D, flags);
+    if (st != ADALN_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
+    TembArgs a{out, K > 1 ? s_out_k : B * S * D, table, table_dtype, temb, temb_dtype, B, S, K, D};
+    return finish_launch(launch_temb_table_slices(a, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
 }
 
 adaln_status adaln_can_residual_gate_add(const void *out, const void *x, const void *gate, int64_t s_gate_b,

@@ -55,6 +55,18 @@ struct GateArgs {
     int64_t B, N, D;
 };
 
+// out_k = table[k] + temb[:, :, k] as K contiguous binary32 slices
+// (dtypes: 0 bf16, 1 fp16, 2 binary32)
+struct TembArgs {
+    void *out;        // slice k at out + k * s_out_k (floats), each (B, S, D)
+    int64_t s_out_k;
+    const void *table;  // (K, D)
+    int table_dtype;
+    const void *temb;   // (B, S, K, D)
+    int temb_dtype;
+    int64_t B, S, K, D;
+};
+
 struct GeluArgs {
     void *out;
     const void *x;
@@ -83,6 +95,7 @@ cudaError_t launch_norm_scale_shift(const LnArgs &a, int dtype, bool pdl, cudaSt
 cudaError_t launch_bias_gelu_tanh(const GeluArgs &a, int dtype, bool pdl, cudaStream_t s,
                                   const DeviceInfo &dev);
 cudaError_t launch_gelu_table_init(void *table, int dtype, cudaStream_t s);
+cudaError_t launch_temb_table_slices(const TembArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 
 // cudaLaunchKernelEx with the optional programmatic-dependent-launch attribute
 template <typename... KArgs, typename... Args>

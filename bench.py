@@ -176,6 +176,7 @@ def make_workloads(dev, which, n_sets=None, flags=0):
     copies rotate so that one pass over them touches at least 4x the L2
     (n_sets=None; at most MAX_SETS copies, so the 133 KB tiny workload stays
     L2-resident: it is launch-bound), or exactly n_sets copies."""
+    import numpy as np
     import torch
 
     import adaln_modulate_gb300 as ad
@@ -276,6 +277,16 @@ def make_workloads(dev, which, n_sets=None, flags=0):
         out["qk_rms"] = ([(lambda t=t: ad.qk_rmsnorm(t[0], t[1], t[2], t[3], 1e-6, q_out=t[4], k_out=t[5],
                                                     flags=flags))
                           for t in copies(base, sets_for(nb))], nb, w.name)
+    if "temb" in which:
+        w = synth.temb_slices()
+        S, K, D = 32760, 6, 3072
+        nb = S * K * D * 2 + K * D * 4 + S * K * D * 4  # temb read, table read, binary32 slices written
+        temb = torch_bits(w.tensors["temb"].draw(), "bf16", dev)
+        table = torch.from_numpy(w.tensors["table"].draw().view(np.uint16).astype(np.uint32) << 16).view(
+            torch.float32).to(dev)  # the bf16 draw widened: a binary32 table
+        base = [temb, table, torch.empty((K, 1, S, D), dtype=torch.float32, device=dev)]
+        out["temb"] = ([(lambda e=e, t=t, o=o: ad.temb_table_slices(t, e, out=o, flags=flags))
+                        for e, t, o in copies(base, sets_for(nb))], nb, w.name)
     for dt in ("bf16", "fp16"):
         key = f"gelu_{dt}"
         if key in which:
@@ -337,6 +348,9 @@ def make_eager(dev, name, nb):
             wq, wk = g((128,), 0.05), g((128,), 0.05)
             out.append(lambda q=q, k=k, wq=wq, wk=wk: (F.rms_norm(q, (128,), wq, 1e-6),
                                                        F.rms_norm(k, (128,), wk, 1e-6)))
+        elif name == "temb":
+            e, t = g((1, 32760, 6, 3072)), g((6, 3072), 0.05).float()
+            out.append(lambda e=e, t=t: [c.contiguous() for c in (t + e.float()).chunk(6, dim=2)])
         elif name.startswith("gelu_"):
             dt = torch.bfloat16 if name == "gelu_bf16" else torch.float16
             x, b = g((32760, 13824)).to(dt), g((13824,), 0.02).to(dt)
@@ -699,7 +713,7 @@ def run_ours(args):
                        "one_stream_ms_per_step": round(serial_ms, 4)}
     if rank == 0 and not args.no_per_config:
         names = ["tiny", "sana", "sana_nmod2", "glm_ln", "glm_gate", "glm_gate_ln", "qk", "gelu_bf16",
-                 "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms"]
+                 "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms", "temb"]
         per = {}
         steps = max(20, min(args.steps, 400))
         for name in names:
@@ -750,7 +764,7 @@ def main():
     p.add_argument("--quick", action="store_true", help="headline only (for profiler runs)")
     p.add_argument("--only", default="sana",
                    choices=["sana", "sana_nmod2", "tiny", "glm_ln", "glm_gate", "glm_gate_ln", "qk",
-                            "gelu_bf16", "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms"],
+                            "gelu_bf16", "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms", "temb"],
                    help="workload timed as the headline (profiling runs); the JSON line's metric "
                         "and roofline describe the Sana LN+modulate only when this is 'sana'")
     args = p.parse_args()

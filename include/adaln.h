@@ -14,6 +14,7 @@
  *                              residual gate, per-sample or per-token rows
  *   adaln_rmsnorm_scale_shift  RMSNorm (no affine) + modulate
  *   adaln_qk_rmsnorm           per-head RMSNorm with a weight on q and k
+ *   adaln_temb_table_slices    table + temb as contiguous binary32 chunks
  *
  * Conventions shared by every call
  * --------------------------------
@@ -60,7 +61,8 @@ typedef enum adaln_status {
 
 typedef enum adaln_dtype {
     ADALN_BF16 = 0,
-    ADALN_FP16 = 1
+    ADALN_FP16 = 1,
+    ADALN_FP32 = 2 /* IEEE binary32: only the inputs of adaln_temb_table_slices */
 } adaln_dtype;
 
 /* norm kinds of adaln_norm_scale_shift */
@@ -213,6 +215,37 @@ adaln_status adaln_can_qk_rmsnorm(const void *q_out, const void *q, int64_t rows
                                   const void *k_out, const void *k, int64_t rows_k,
                                   int64_t Dh, const void *wq, const void *wk,
                                   float eps, int dtype, uint32_t flags);
+
+/* ------------------------------------------------------------------------
+ * adaln_temb_table_slices
+ *   out_k[b, s, :] = table[k, :] + temb[b, s, k, :]      k = 0 .. K-1
+ *
+ * The "temb_table_slices" of the Fused Kernels page (adaLN modulation and
+ * gating table and its note): the eager (scale_shift_table +
+ * temb.float()).chunk(K, dim=2) as K slices, each contiguous, written in
+ * one pass (no full binary32 sum materialised and no .contiguous() copies).
+ *   out    binary32; slice k is the contiguous (B, S, D) block at
+ *          out + k * s_out_k (floats); s_out_k >= B*S*D (ignored for K = 1).
+ *   table  (K, D) contiguous, table_dtype ADALN_BF16 / ADALN_FP16 / ADALN_FP32.
+ *   temb   (B, S, K, D) contiguous (S = 1 for one row per sample),
+ *          temb_dtype likewise.
+ *   Limits: B, S, K, D >= 1; K, D <= 65536.  out overlaps neither input.
+ *   Pointers aligned to their element size; 8-wide accesses when D % 8 ==
+ *   0, s_out_k % 8 == 0, out 32-byte and the inputs 8-element aligned,
+ *   one element per access otherwise (same bits).
+ * Numerics: one IEEE binary32 addition of the exactly promoted operands.
+ * Returns ADALN_E_DTYPE for a dtype outside the three, ADALN_E_STRIDE for
+ * s_out_k < B*S*D, and the common statuses.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_temb_table_slices(void *out, int64_t s_out_k, const void *table, int table_dtype,
+                                    const void *temb, int temb_dtype,
+                                    int64_t B, int64_t S, int64_t K, int64_t D,
+                                    uint32_t flags, void *stream);
+
+adaln_status adaln_can_temb_table_slices(const void *out, int64_t s_out_k, const void *table,
+                                        int table_dtype, const void *temb, int temb_dtype,
+                                        int64_t B, int64_t S, int64_t K, int64_t D,
+                                        uint32_t flags);
 
 /* ------------------------------------------------------------------------
  * adaln_residual_gate_add

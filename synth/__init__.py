@@ -197,6 +197,15 @@ def qk_rms(N: int = 4096, H: int = 30) -> Workload:
     }, {"eps": 1e-6})
 
 
+def temb_slices(S: int = 32760, K: int = 6, D: int = 3072) -> Workload:
+    """A per-token modulation input: temb (1, S, K, D) bf16 and a binary32
+    (K, D) table, the shape of the Wan FFN workload's tokens at width 3072."""
+    return Workload(f"temb_table_slices (1,{S},{K},{D}) bf16 temb, binary32 table", "temb_table_slices", {
+        "temb": TensorSpec((1, S, K, D), 0.0, 1.0, SEEDS["x"]),
+        "table": TensorSpec((K, D), 0.0, 0.05, SEEDS["table"]),
+    })
+
+
 def all_workloads() -> List[Workload]:
     return [ln_tiny(), ln_sana(), ln_glm(), gate_add_glm(), qk_glm(), gelu_wan("bf16"),
-            gelu_wan("fp16"), rms_rows(), rms_tokens(), gate_rms_tokens(), qk_rms()]
+            gelu_wan("fp16"), rms_rows(), rms_tokens(), gate_rms_tokens(), qk_rms(), temb_slices()]

@@ -183,3 +183,36 @@ def test_qk_rmsnorm_validation(ad):
     assert f(QO, Q, 100, KO, K, 100, 128, W, W + 256, 1e-6, 0, 0) == 0
     assert f(W, Q, 100, KO, K, 100, 128, W, W + 256, 1e-6, 0, 0) == 7   # q_out on the weight
     assert f(QO, Q, 100, KO, K, 100, 128, W + 4, W + 256, 1e-6, 0, 0) == 4
+
+
+def test_temb_table_slices_validation(ad):
+    f = ad.capi.adaln_can_temb_table_slices
+    O, T, E = 1 << 36, 1 << 37, 1 << 38
+    B, S, K, D = 1, 100, 6, 3072
+    ok = (O, B * S * D, T, 2, E, 0, B, S, K, D, 0)
+    assert f(*ok) == 0
+    a = list(ok)
+    a[3] = 3
+    assert f(*a) == 2                              # table dtype
+    a = list(ok)
+    a[5] = -1
+    assert f(*a) == 2                              # temb dtype
+    a = list(ok)
+    a[1] = B * S * D - 8
+    assert f(*a) == 5                              # slices would overlap
+    a = list(ok)
+    a[0] = O + 2
+    assert f(*a) == 4                              # out not 4-byte aligned
+    a = list(ok)
+    a[0] = E + 64
+    assert f(*a) == 7                              # out over temb
+    a = list(ok)
+    a[2] = O + 4 * (B * S * D * 5 + 8)
+    assert f(*a) == 7                              # table inside the last slice
+    a = list(ok)
+    a[9] = 0
+    assert f(*a) == 3
+    a = list(ok)
+    a[10] = 2
+    assert f(*a) == 6
+    assert f(O, 0, T, 0, E, 1, 2, 3, 1, 8, 0) == 0  # K = 1 ignores the slice stride
