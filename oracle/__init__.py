@@ -22,6 +22,10 @@ Parity status of each function (what pins it, see ``tests/test_oracle_*``):
   qk_rmsnorm         pinned: fp64 RMSNorm with weight, exact rows
   temb_table_slices  pinned: numpy's binary32 addition of the promoted
                      operands, slice by slice
+  e4m3 / quant_e4m3  pinned: torch's float8_e4m3fn rounding of clamped
+                     values (every bf16 and fp16 pattern, tie cases),
+                     exhaustive decode round trip; ln_modulate_fp8 is the
+                     pinned LN+modulate followed by the pinned quantiser
   bias_gelu_tanh     pinned: 100-bit evaluation of tanh-GELU on all inputs
   rsqrt_cr           pinned: 100-bit evaluation
 """
@@ -85,12 +89,14 @@ def _lib_handle():
                                             _P, _I, _I, _P, _I, _I, _F, _INT, _I, _I, _P, _P],
                 "oracle_qk_rmsnorm": [_P, _P, _I, _I, _P, _F, _INT, _I, _I],
                 "oracle_temb_table_slices": [_P, _I, _P, _INT, _P, _INT, _I, _I, _I, _I],
+                "oracle_quant_e4m3": [_P, _P, _I, _F, _INT],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
             for name, args in {"oracle_f32_to_16": [_P, _P, _I, _INT],
+                               "oracle_f32_to_e4m3_array": [_P, _P, _I],
                                "oracle_16_to_f32": [_P, _P, _I, _INT],
                                "oracle_rsqrt_cr_array": [_P, _P, _I]}.items():
                 fn = getattr(lib, name)
@@ -396,6 +402,38 @@ def temb_table_slices(table: np.ndarray, table_dtype: str, temb: np.ndarray, tem
     if rc:
         raise ValueError("oracle_temb_table_slices rejected its arguments")
     return out
+
+
+def quant_e4m3(y: np.ndarray, qscale: float, dtype: str = "bf16") -> np.ndarray:
+    """Static FP8 quantisation of storage values: e4m3(value(y) / qscale),
+    binary32 division, round to nearest even, saturating at 448 (the
+    Quantized layout producers table's static FP8 output).  Returns uint8."""
+    yf = np.ascontiguousarray(_u16(y))
+    out = np.zeros(yf.shape, dtype=np.uint8)
+    _lib_handle().oracle_quant_e4m3(out.ctypes.data, yf.ctypes.data, yf.size, float(np.float32(qscale)),
+                                    DTYPE_CODE[dtype])
+    return out
+
+
+def e4m3(f: np.ndarray) -> np.ndarray:
+    """binary32 values -> e4m3 codes (round to nearest even, saturating)."""
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    out = np.empty(f.shape, dtype=np.uint8)
+    _lib_handle().oracle_f32_to_e4m3_array(f.ctypes.data, out.ctypes.data, f.size)
+    return out
+
+
+def ln_modulate_fp8(x_base: np.ndarray, B: int, N: int, D: int, strides: Tuple[int, int, int],
+                    scale_base: np.ndarray, scale_offset: int, s_scale_b: int,
+                    shift_base: np.ndarray, shift_offset: int, s_shift_b: int, eps: float, qscale: float,
+                    dtype: str = "bf16", rows: Optional[Sequence[int]] = None, threads: int = 1):
+    """LayerNorm + adaLN modulate written as static FP8: ln_modulate's
+    storage output quantised by quant_e4m3 (Fused Kernels page, Quantized
+    layout producers table: flux2_layernorm_modulate_fp8_quant).  Returns
+    (row_ids, uint8 codes (rows, D))."""
+    ids, y = ln_modulate(x_base, B, N, D, strides, scale_base, scale_offset, s_scale_b, shift_base, shift_offset,
+                         s_shift_b, eps, dtype, rows=rows, threads=threads)
+    return ids, quant_e4m3(y, qscale, dtype)
 
 
 def bias_gelu_tanh(x: np.ndarray, bias: np.ndarray, rows_total: int, width: int,

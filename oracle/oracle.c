@@ -33,6 +33,9 @@
  *  - temb_table_slices: "Fused Kernels", adaLN modulation and gating table
  *    and its note on the op ((scale_shift_table + temb.float()).chunk(6)
  *    into six contiguous slices in one pass).
+ *  - static FP8 output of LN + modulate: "Fused Kernels", Quantized layout
+ *    producers table (flux2_layernorm_modulate_fp8_quant: LayerNorm plus
+ *    adaLN modulation directly into static FP8 output).
  *
  * Readings where the pages leave a step open (each also listed in the design
  * notes): the reciprocal in the Welford push and every division are IEEE
@@ -509,6 +512,52 @@ int oracle_temb_table_slices(float *out, int64_t s_out_k, const void *table, int
                 out[k * s_out_k + bs * D + d] =
                     load_any(table, k * D + d, table_dtype) + load_any(temb, (bs * K + k) * D + d, temb_dtype);
     return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* static FP8 (e4m3, finite-only) quantisation                          */
+/* ------------------------------------------------------------------ */
+
+/* binary32 -> fp8 e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; no infinities; 0x7F / 0xFF are NaN; largest finite 448), round to
+ * nearest even with saturation: |f| beyond 448, infinities included, give
+ * +-448; NaN gives 0x7F.  Written from the format definition: the result is
+ * the nearest multiple of the quantum of f's binade (2^(e-3) for
+ * 2^e <= |f| < 2^(e+1), e >= -6; 2^-9 below 2^-6), ties to the even
+ * multiple. */
+static uint8_t f32_to_e4m3_sat(float f) {
+    if (isnan(f)) return 0x7f;
+    uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a >= 448.0) return sign | 0x7e;
+    int e;
+    frexp(a, &e);                 /* a = m * 2^e, m in [0.5, 1) (a > 0) */
+    int ex = (a == 0.0) ? -6 : e - 1;
+    if (ex < -6) ex = -6;         /* subnormal quantum 2^-9 */
+    double quantum = ldexp(1.0, ex - 3);
+    double q = a / quantum;       /* exact: a has 24 significant bits */
+    double r = floor(q), frac = q - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    double v = r * quantum;       /* <= 448: values from 448 up returned above */
+    if (v == 0.0) return sign;
+    int ve;
+    frexp(v, &ve);
+    int E = ve - 1;               /* binade of the rounded value */
+    if (E < -6) return sign | (uint8_t)(v / ldexp(1.0, -9));            /* subnormal code */
+    int mant = (int)(v / ldexp(1.0, E - 3)) - 8;                        /* 0..7 */
+    return sign | (uint8_t)(((E + 7) << 3) | mant);
+}
+
+/* out8[i] = e4m3(value(y[i]) / qscale), y storage values (dtype 0 bf16,
+ * 1 fp16), one IEEE binary32 division, then f32_to_e4m3_sat. */
+int oracle_quant_e4m3(uint8_t *out8, const uint16_t *y, int64_t n, float qscale, int dtype) {
+    for (int64_t i = 0; i < n; ++i) out8[i] = f32_to_e4m3_sat(load16(y[i], dtype) / qscale);
+    return 0;
+}
+
+/* every binary32 input of a pin through the encoder */
+void oracle_f32_to_e4m3_array(const float *in, uint8_t *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_e4m3_sat(in[i]);
 }
 
 /* ------------------------------------------------------------------ */

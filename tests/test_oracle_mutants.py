@@ -24,6 +24,7 @@ import oracle
 import test_oracle_ln as ln
 import test_oracle_qk_gate_gelu as qg
 import test_oracle_rms as rm
+import test_oracle_fp8 as f8
 import test_oracle_temb as tb
 import test_oracle_rsqrt as rs
 import test_oracle_conversions as cv
@@ -69,6 +70,12 @@ MUTANTS = {
     "temb_chunk_major_layout": ("load_any(temb, (bs * K + k) * D + d, temb_dtype)",
                                 "load_any(temb, (k * B * S + bs) * D + d, temb_dtype)"),
     "temb_table_row_zero": ("load_any(table, k * D + d, table_dtype)", "load_any(table, d, table_dtype)"),
+    "e4m3_ties_away_from_zero": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;",
+                                 "if (frac >= 0.5) r += 1.0;"),
+    "e4m3_no_saturation": ("if (a >= 448.0) return sign | 0x7e;", "if (a >= 4480.0) return sign | 0x7e;"),
+    "e4m3_subnormal_quantum": ("if (ex < -6) ex = -6;", "if (ex < -7) ex = -7;"),
+    "quant_by_reciprocal": ("f32_to_e4m3_sat(load16(y[i], dtype) / qscale)",
+                            "f32_to_e4m3_sat(load16(y[i], dtype) * (1.0f / qscale))"),
     "temb_slice_stride_ignored": ("out[k * s_out_k + bs * D + d] =", "out[k * B * S * D / K + bs * D + d] ="),
     "gelu_constant_typo": ("const long double k1 = 0.044715L;", "const long double k1 = 0.04715L;"),
     "gelu_sign": ("long double g = v / (1.0L + expl(-2.0L * z));", "long double g = v / (1.0L + expl(2.0L * z));"),
@@ -129,6 +136,10 @@ def _pins():
     P.append(("qk_rms_exact", lambda: rm.test_qk_rms_exact_rows(None, 64)))
     P.append(("temb_add", lambda: tb.test_slices_equal_numpy_binary32_add(None, "fp32", "bf16")))
     P.append(("temb_order", lambda: tb.test_slice_order_and_broadcast(None)))
+    P.append(("e4m3_round_trip", lambda: f8.test_every_code_round_trips(None)))
+    P.append(("e4m3_ties", lambda: f8.test_ties_saturation_nan_and_zero(None)))
+    P.append(("e4m3_torch", lambda: f8.test_quantiser_matches_torch_on_every_pattern(None, "bf16", 0.37)))
+    P.append(("e4m3_div_ties", lambda: f8.test_exact_ties_after_division(None)))
     P.append(("bf16_encode", lambda: cv.test_bf16_encode_vs_torch(None)))
     P.append(("fp16_encode", lambda: cv.test_fp16_encode_vs_numpy(None)))
     return P
