@@ -10,8 +10,9 @@ Two layers:
     and so on), taking raw integers (device pointers, sizes, a stream handle);
   * ``ln_modulate``, ``qk_head_layernorm``, ``residual_gate_add``,
     ``bias_gelu_tanh``, ``residual_gate_ln_modulate``, ``norm_scale_shift``,
-    ``rmsnorm_scale_shift``, ``qk_rmsnorm``, ``temb_table_slices``: the same calls taking torch
-    tensors (PyTorch only provides the device memory and the current stream).
+    ``rmsnorm_scale_shift``, ``qk_rmsnorm``, ``temb_table_slices``,
+    ``ln_modulate_fp8``: the same calls taking torch tensors (PyTorch only
+    provides the device memory and the current stream).
 """
 from __future__ import annotations
 
@@ -74,6 +75,9 @@ _SIGS = {
     "adaln_qk_rmsnorm": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _F, _INT, _U, _P], _INT),
     "adaln_can_qk_rmsnorm": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _F, _INT, _U], _INT),
     "adaln_temb_table_slices": ([_P, _I, _P, _INT, _P, _INT, _I, _I, _I, _I, _U, _P], _INT),
+    "adaln_ln_modulate_fp8": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U, _P], _INT),
+    "adaln_can_ln_modulate_fp8": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U], _INT),
+    "adaln_ln_modulate_fp8_variant": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U], _INT),
     "adaln_can_temb_table_slices": ([_P, _I, _P, _INT, _P, _INT, _I, _I, _I, _I, _U], _INT),
 }
 
@@ -169,6 +173,44 @@ def ln_modulate(x, scale, shift, eps: float, out=None, flags: int = 0, stream=No
                                 hsb, float(eps), _dtype_code(x), flags, _stream(stream))
     _check(st, "adaln_ln_modulate")
     return out
+
+
+def _fp8_args(x, scale, shift, qscale):
+    B, N, D = x.shape
+    rows = []
+    for t, name in ((scale, "scale"), (shift, "shift")):
+        p, sb = _rows_view(t, D, name)
+        if t.shape[0] not in (1, B):
+            raise ValueError(f"{name} batch must be 1 or B")
+        rows.append((p, 0 if t.shape[0] == 1 else sb))
+    if qscale.numel() != 1 or qscale.dtype != _torch().float32:
+        raise ValueError("qscale must be one float32 value on the device")
+    return B, N, D, rows
+
+
+def ln_modulate_fp8(x, scale, shift, eps: float, qscale, out=None, flags: int = 0, stream=None):
+    """``e4m3((LN(x) * (1 + scale) + shift) / qscale)`` (static FP8) for x
+    (B, N, D) of any strides; scale / shift as ln_modulate; qscale a float32
+    device tensor of one element.  Returns a (B, N, D) torch.float8_e4m3fn
+    tensor (or writes ``out``, uint8 or float8_e4m3fn)."""
+    torch = _torch()
+    B, N, D, ((sp, ssb), (hp, hsb)) = _fp8_args(x, scale, shift, qscale)
+    if out is None:
+        out = torch.empty((B, N, D), dtype=torch.float8_e4m3fn, device=x.device)
+    st = capi.adaln_ln_modulate_fp8(out.data_ptr(), qscale.data_ptr(), x.data_ptr(), B, N, D, *x.stride(), sp, ssb,
+                                    hp, hsb, float(eps), _dtype_code(x), flags, _stream(stream))
+    _check(st, "adaln_ln_modulate_fp8")
+    return out
+
+
+def ln_modulate_fp8_variant(x, scale, shift, eps: float, qscale) -> str:
+    """Which kernel ln_modulate_fp8 takes for these tensors (no CUDA work)."""
+    B, N, D, ((sp, ssb), (hp, hsb)) = _fp8_args(x, scale, shift, qscale)
+    v = capi.adaln_ln_modulate_fp8_variant(1 << 40, qscale.data_ptr(), x.data_ptr(), B, N, D, *x.stride(), sp, ssb,
+                                           hp, hsb, float(eps), _dtype_code(x), 0)
+    if v < 0:
+        raise AdalnError(-v, "adaln_ln_modulate_fp8_variant")
+    return VARIANTS[v]
 
 
 def tma_wait_timeouts() -> int:

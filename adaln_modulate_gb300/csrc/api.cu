@@ -251,6 +251,26 @@ LnArgs norm_args(int norm, void *r_out, void *out, const void *x, int64_t B, int
     return a;
 }
 
+// LayerNorm + modulate into static FP8: check_ln's rules with 1-byte outputs
+adaln_status check_ln_fp8(const void *out, const void *qscale, const void *x, int64_t B, int64_t N, int64_t D,
+                          int64_t sxB, int64_t sxN, int64_t sxD, const void *scale, int64_t s_scale_b,
+                          const void *shift, int64_t s_shift_b, float eps, int dtype, uint32_t flags) {
+    if (dtype != ADALN_BF16 && dtype != ADALN_FP16) return ADALN_E_DTYPE;
+    if (flags & ~ADALN_FLAG_PDL) return ADALN_E_VALUE;
+    if (!out || !qscale || !x || !scale || !shift) return ADALN_E_NULL;
+    if (B < 1 || N < 1 || D < 4 || D > 65536 || D % 4 != 0) return ADALN_E_SHAPE;
+    if (B > ((int64_t)1 << 40) / N || B * N > ((int64_t)1 << 46) / D) return ADALN_E_SHAPE;
+    if (sxB < 0 || sxN < 0 || sxD < 0 || s_scale_b < 0 || s_shift_b < 0) return ADALN_E_STRIDE;
+    if (!finite_nonneg(eps)) return ADALN_E_VALUE;
+    if (!al2(x) || !al2(scale) || !al2(shift) || ((uintptr_t)qscale & 3u)) return ADALN_E_ALIGN;
+    const int64_t nb = B * N * D;
+    if (overlap(out, nb, x, extent(B, N, D, sxB, sxN, sxD)) ||
+        overlap(out, nb, scale, extent(B, 1, D, s_scale_b, 0, 1)) ||
+        overlap(out, nb, shift, extent(B, 1, D, s_shift_b, 0, 1)) || overlap(out, nb, qscale, 4))
+        return ADALN_E_OVERLAP;
+    return ADALN_OK;
+}
+
 adaln_status check_temb(const void *out, int64_t s_out_k, const void *table, int table_dtype, const void *temb,
                         int temb_dtype, int64_t B, int64_t S, int64_t K, int64_t D, uint32_t flags) {
     auto ok_dt = [](int d) { return d == ADALN_BF16 || d == ADALN_FP16 || d == ADALN_FP32; };
@@ -533,6 +553,40 @@ adaln_status adaln_qk_rmsnorm(void *q_out, const void *q, int64_t rows_q, void *
     QkArgs a{q_out, q, rows_q, k_out, k, rows_k, Dh, wq, nullptr, wk, nullptr, eps, true};
     return finish_launch(
         launch_qk_head_layernorm(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
+}
+
+adaln_status adaln_can_ln_modulate_fp8(const void *out, const void *qscale, const void *x, int64_t B, int64_t N,
+                                      int64_t D, int64_t sxB, int64_t sxN, int64_t sxD, const void *scale,
+                                      int64_t s_scale_b, const void *shift, int64_t s_shift_b, float eps, int dtype,
+                                      uint32_t flags) {
+    return check_ln_fp8(out, qscale, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps, dtype,
+                        flags);
+}
+
+int adaln_ln_modulate_fp8_variant(const void *out, const void *qscale, const void *x, int64_t B, int64_t N, int64_t D,
+                                  int64_t sxB, int64_t sxN, int64_t sxD, const void *scale, int64_t s_scale_b,
+                                  const void *shift, int64_t s_shift_b, float eps, int dtype, uint32_t flags) {
+    adaln_status st = check_ln_fp8(out, qscale, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps,
+                                   dtype, flags);
+    if (st != ADALN_OK) return -(int)st;
+    LnArgs a{(void *)out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps};
+    a.qscale = (const float *)qscale;
+    return ln_modulate_path(a);
+}
+
+adaln_status adaln_ln_modulate_fp8(void *out, const void *qscale, const void *x, int64_t B, int64_t N, int64_t D,
+                                  int64_t sxB, int64_t sxN, int64_t sxD, const void *scale, int64_t s_scale_b,
+                                  const void *shift, int64_t s_shift_b, float eps, int dtype, uint32_t flags,
+                                  void *stream) {
+    adaln_status st = check_ln_fp8(out, qscale, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps,
+                                   dtype, flags);
+    if (st != ADALN_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev)) != ADALN_OK || (st = device_info(dev, &info)) != ADALN_OK) return st;
+    LnArgs a{out, x, B, N, D, sxB, sxN, sxD, scale, s_scale_b, shift, s_shift_b, eps};
+    a.qscale = (const float *)qscale;
+    return finish_launch(launch_norm_scale_shift(a, dtype, (flags & ADALN_FLAG_PDL) != 0, (cudaStream_t)stream, info));
 }
 
 adaln_status adaln_can_temb_table_slices(const void *out, int64_t s_out_k, const void *table, int table_dtype,

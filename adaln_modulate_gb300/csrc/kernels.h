@@ -31,6 +31,7 @@ struct LnArgs {
     int64_t s_gate_b = 0, s_gate_n = 0, s_gate_d = 1;
     const void *y = nullptr;               // with a gate: y and r_out contiguous (B, N, D), x too
     void *r_out = nullptr;
+    const float *qscale = nullptr;         // set: out is e4m3 bytes, e4m3(y / *qscale) (static FP8)
 };
 
 struct QkArgs {

@@ -207,6 +207,8 @@ ADALN_ROWS_DECL(rows_rms_bf16)
 ADALN_ROWS_DECL(rows_rms_fp16)
 ADALN_ROWS_DECL(rows_rms_gate_bf16)
 ADALN_ROWS_DECL(rows_rms_gate_fp16)
+ADALN_ROWS_DECL(rows_ln_fp8_bf16)  // LayerNorm, no gate, static FP8 output
+ADALN_ROWS_DECL(rows_ln_fp8_fp16)
 #undef ADALN_ROWS_DECL
 cudaError_t ln_tokens_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);
 cudaError_t ln_generic_launch(const LnArgs &a, int dtype, bool pdl, cudaStream_t s, const DeviceInfo &dev);

@@ -3,6 +3,8 @@
 // one CTA of 128 threads per row, thread l is logical lane l, scalar loads,
 // plain binary32 code.  The path of last resort behind the rows and tokens
 // kernels; same DAG, same bits.
+#include <cuda_fp8.h>
+
 #include "ln_common.cuh"
 
 namespace adaln {
@@ -20,6 +22,7 @@ struct GenericParams {
     int64_t s_gate_b, s_gate_n, s_gate_d;
     const uint16_t *y;
     uint16_t *r_out;
+    const float *qscale;  // set: out holds e4m3 bytes, e4m3(y / *qscale)
 };
 
 // Pass 1 reads x (and y, gate), forms v (r = round(x + round(gate * y)) with
@@ -37,6 +40,7 @@ ln_generic_kernel(const GenericParams p) {
     const float Df = (float)D;
     pdl_wait();
     pdl_trigger();
+    const float qs = p.qscale ? *p.qscale : 1.0f;
     for (int64_t row = blockIdx.x; row < p.B * p.N; row += gridDim.x) {
         const int64_t b = row / p.N, n = row - b * p.N;
         const uint16_t *xr = p.x + b * p.sxB + n * p.sxN;
@@ -99,7 +103,14 @@ ln_generic_kernel(const GenericParams p) {
                 const float y = h_f32<T>(to16_rn<T>(__fmul_rn(rstd, __fsub_rn(v, mean))));
                 const float op = h_f32<T>(to16_rn<T>(__fadd_rn(1.0f, h_f32<T>(scr[d]))));
                 const float pr = h_f32<T>(to16_rn<T>(__fmul_rn(y, op)));
-                orow[d] = to16_rn<T>(__fadd_rn(pr, h_f32<T>(shr[d])));
+                const uint16_t o16 = to16_rn<T>(__fadd_rn(pr, h_f32<T>(shr[d])));
+                if (p.qscale) {
+                    const float q = __fdiv_rn(h_f32<T>(o16), qs);
+                    reinterpret_cast<uint8_t *>(p.out)[row * D + d] =
+                        (uint8_t)__nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
+                } else {
+                    orow[d] = o16;
+                }
             }
         __syncthreads();  // xch / fin are reused by the next row
     }
@@ -114,7 +125,7 @@ static cudaError_t run_generic(const LnArgs &a, bool pdl, cudaStream_t s, const 
                     (const uint16_t *)a.scale, a.s_scale_b, a.s_scale_n,
                     (const uint16_t *)a.shift, a.s_shift_b, a.s_shift_n, a.eps,
                     (const uint16_t *)a.gate, a.s_gate_b, a.s_gate_n, a.s_gate_d,
-                    (const uint16_t *)a.y, (uint16_t *)a.r_out};
+                    (const uint16_t *)a.y, (uint16_t *)a.r_out, a.qscale};
     return launch_k(k, dim3((unsigned)grid), dim3(128), 0, s, pdl, p);
 }
 

@@ -26,8 +26,11 @@
 // the output pass is the LayerNorm's with mean 0), per-token modulation
 // rows (the strided [B, S, 6D] chunk views of the request-gated fusion
 // table) and the residual gate-add in front (scale_residual_norm_scale_shift,
-// with a per-sample gate row or a per-token [B, S, 1] gate); the tokens
-// kernels take only the LayerNorm with per-sample rows and no gate.
+// with a per-sample gate row or a per-token [B, S, 1] gate), and the static
+// FP8 output of the Quantized layout producers table
+// (flux2_layernorm_modulate_fp8_quant: e4m3(y / scale) of every output y);
+// the tokens kernels take only the LayerNorm with per-sample rows, no gate
+// and storage output.
 #include "ln_common.cuh"
 
 namespace adaln {
@@ -50,11 +53,13 @@ bool ln_rows_ok(const LnArgs &a) {
 
 int ln_modulate_path(const LnArgs &a) {
     const int64_t ni = (a.D + 511) / 512;
-    if (a.sxD == 1 && ni <= kRowsMaxNI && ln_rows_ok(a)) return LN_PATH_ROWS;
+    // the static FP8 output has rows kernels for the gate-free LayerNorm only
+    const bool rows_kind = !a.qscale || (a.norm == 0 && !a.gate);
+    if (rows_kind && a.sxD == 1 && ni <= kRowsMaxNI && ln_rows_ok(a)) return LN_PATH_ROWS;
     // tokens contiguous (LayerNorm, one scale / shift row per sample, no
-    // gate): each d-row of 8 tokens is one 16-byte copy
+    // gate, storage output): each d-row of 8 tokens is one 16-byte copy
     const bool per_sample = a.s_scale_n == 0 && a.s_shift_n == 0;
-    if (a.norm == 0 && !a.gate && per_sample && a.sxN == 1 && a.sxD != 1 && a.N > 1 && ni <= kTokensMaxNI &&
+    if (a.norm == 0 && !a.gate && !a.qscale && per_sample && a.sxN == 1 && a.sxD != 1 && a.N > 1 && ni <= kTokensMaxNI &&
         ln_aligned(a.x, 16) && ln_mult(a.sxD, 8) &&
         (a.B == 1 || (ln_mult(a.sxB, 8) && ln_mult(a.s_scale_b, 4) && ln_mult(a.s_shift_b, 4))) &&
         ln_aligned(a.out, 8) && ln_aligned(a.scale, 8) && ln_aligned(a.shift, 8))
@@ -69,6 +74,7 @@ cudaError_t launch_norm_scale_shift(const LnArgs &a, int dtype, bool pdl, cudaSt
             static const RowsFn fns[2][2][2] = {  // [norm][gate][dtype]
                 {{rows_ln_bf16, rows_ln_fp16}, {rows_ln_gate_bf16, rows_ln_gate_fp16}},
                 {{rows_rms_bf16, rows_rms_fp16}, {rows_rms_gate_bf16, rows_rms_gate_fp16}}};
+            if (a.qscale) return dtype == 0 ? rows_ln_fp8_bf16(a, pdl, s, dev) : rows_ln_fp8_fp16(a, pdl, s, dev);
             return fns[a.norm == 1][a.gate != nullptr][dtype != 0](a, pdl, s, dev);
         }
         case LN_PATH_TOKENS: return ln_tokens_launch(a, dtype, pdl, s, dev);

@@ -45,6 +45,10 @@ constexpr int kOpshMaxBytes = 32 * 1024;
 // sample and join the shared table after the op / shift pairs (B * D * 2
 // more bytes; the whole table stays within kOpshMaxBytes).
 enum GateMode : int { GATE_NONE = 0, GATE_ROW = 1, GATE_SCALAR = 2 };
+
+// E4M3: the output is static FP8, e4m3(y / *qscale) of each storage value
+// y of the chain (binary32 division, round to nearest even, saturating at
+// +-448): one byte per element, 4 per lane chunk.
 struct RowsParams {
     uint16_t *out;
     const uint16_t *x;
@@ -60,9 +64,10 @@ struct RowsParams {
     const uint16_t *gate;
     int64_t s_gate_b, s_gate_n;
     uint16_t *r_out;
+    const float *qscale;
 };
 
-template <DT T, int NI, bool TAIL, bool OPSH, int GM, bool RMS>
+template <DT T, int NI, bool TAIL, bool OPSH, int GM, bool RMS, bool E4M3 = false>
 __global__ void __launch_bounds__(kRowsThreads, 2)
 ln_rows_kernel(const RowsParams p) {
     constexpr bool GATE = GM != GATE_NONE;
@@ -80,6 +85,8 @@ ln_rows_kernel(const RowsParams p) {
     __syncthreads();
     pdl_wait();
     pdl_trigger();
+    QuantE4M3 qc{};  // E4M3: the static scale (written by earlier work on the stream) and its constants
+    if constexpr (E4M3) qc = quant_setup<T>(*p.qscale);
     const int u = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int D = p.D;
@@ -258,6 +265,7 @@ ln_rows_kernel(const RowsParams p) {
         const uint16_t *shr = p.shift + b * p.s_shift_b + n * p.s_shift_n + c0;
         const uint32_t *ob = opsh + b * D + c0;  // OPSH: (op, shift) of the column pairs from c0 on
         uint16_t *orow = p.out + row * (int64_t)D + c0;
+        uint8_t *orow8 = reinterpret_cast<uint8_t *>(p.out) + row * (int64_t)D + c0;  // E4M3
         const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
@@ -287,7 +295,11 @@ ln_rows_kernel(const RowsParams p) {
                         f2_split(f2_mul(f2_sub(f2(xl, xh), mm), rr), y0, y1);
                         o[k] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0, y1), op[k]), sh[k]);
                     }
-                    st8(orow + off, o);
+                    if constexpr (E4M3) {
+                        st4(orow8 + off, quant4_e4m3<T>(o, qc));
+                    } else {
+                        st8(orow + off, o);
+                    }
                 }
             }
         }
@@ -311,9 +323,9 @@ static inline int rows_gate_mode(const LnArgs &a) {
     return !a.gate ? GATE_NONE : (a.s_gate_d == 0 ? GATE_SCALAR : GATE_ROW);
 }
 
-template <DT T, int NI, bool TAIL, bool OPSH, int GM, bool RMS>
+template <DT T, int NI, bool TAIL, bool OPSH, int GM, bool RMS, bool E4M3>
 static cudaError_t run_rows(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
-    auto k = ln_rows_kernel<T, NI, TAIL, OPSH, GM, RMS>;
+    auto k = ln_rows_kernel<T, NI, TAIL, OPSH, GM, RMS, E4M3>;
     // <= kOpshMaxBytes with OPSH (rows_opsh_ok), which leaves room for the
     // static shared memory under the 48 KiB a launch gets without opt-in
     const size_t smem = OPSH ? (size_t)rows_opsh_bytes(a, GM) : 0;
@@ -324,31 +336,31 @@ static cudaError_t run_rows(const LnArgs &a, bool pdl, cudaStream_t s, const Dev
                  (const uint16_t *)a.scale, a.s_scale_b, a.N == 1 ? 0 : a.s_scale_n,
                  (const uint16_t *)a.shift, a.s_shift_b, a.N == 1 ? 0 : a.s_shift_n, a.eps,
                  (const uint16_t *)a.y, (const uint16_t *)a.gate, a.s_gate_b, a.N == 1 ? 0 : a.s_gate_n,
-                 (uint16_t *)a.r_out};
+                 (uint16_t *)a.r_out, a.qscale};
     return launch_k(k, dim3((unsigned)grid), dim3(kRowsThreads), smem, s, pdl, p);
 }
 
-template <DT T, int NI, int GM, bool RMS>
+template <DT T, int NI, int GM, bool RMS, bool E4M3>
 static cudaError_t rows_tail(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     const bool tail = a.D % 512 != 0;
     if (rows_opsh_ok(a, GM))
-        return tail ? run_rows<T, NI, true, true, GM, RMS>(a, pdl, s, dev)
-                    : run_rows<T, NI, false, true, GM, RMS>(a, pdl, s, dev);
-    return tail ? run_rows<T, NI, true, false, GM, RMS>(a, pdl, s, dev)
-                : run_rows<T, NI, false, false, GM, RMS>(a, pdl, s, dev);
+        return tail ? run_rows<T, NI, true, true, GM, RMS, E4M3>(a, pdl, s, dev)
+                    : run_rows<T, NI, false, true, GM, RMS, E4M3>(a, pdl, s, dev);
+    return tail ? run_rows<T, NI, true, false, GM, RMS, E4M3>(a, pdl, s, dev)
+                : run_rows<T, NI, false, false, GM, RMS, E4M3>(a, pdl, s, dev);
 }
 
-template <DT T, int GM, bool RMS>
+template <DT T, int GM, bool RMS, bool E4M3 = false>
 static cudaError_t rows_vec(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     switch ((a.D + 511) / 512) {
-        case 1: return rows_tail<T, 1, GM, RMS>(a, pdl, s, dev);
-        case 2: return rows_tail<T, 2, GM, RMS>(a, pdl, s, dev);
-        case 3: return rows_tail<T, 3, GM, RMS>(a, pdl, s, dev);
-        case 4: return rows_tail<T, 4, GM, RMS>(a, pdl, s, dev);
-        case 5: return rows_tail<T, 5, GM, RMS>(a, pdl, s, dev);
-        case 6: return rows_tail<T, 6, GM, RMS>(a, pdl, s, dev);
-        case 7: return rows_tail<T, 7, GM, RMS>(a, pdl, s, dev);
-        case 8: return rows_tail<T, 8, GM, RMS>(a, pdl, s, dev);
+        case 1: return rows_tail<T, 1, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 2: return rows_tail<T, 2, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 3: return rows_tail<T, 3, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 4: return rows_tail<T, 4, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 5: return rows_tail<T, 5, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 6: return rows_tail<T, 6, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 7: return rows_tail<T, 7, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 8: return rows_tail<T, 8, GM, RMS, E4M3>(a, pdl, s, dev);
     }
     return cudaErrorInvalidValue;
 }

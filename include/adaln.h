@@ -15,6 +15,7 @@
  *   adaln_rmsnorm_scale_shift  RMSNorm (no affine) + modulate
  *   adaln_qk_rmsnorm           per-head RMSNorm with a weight on q and k
  *   adaln_temb_table_slices    table + temb as contiguous binary32 chunks
+ *   adaln_ln_modulate_fp8      LayerNorm + adaLN modulate into static FP8
  *
  * Conventions shared by every call
  * --------------------------------
@@ -214,6 +215,52 @@ adaln_status adaln_qk_rmsnorm(void *q_out, const void *q, int64_t rows_q,
 adaln_status adaln_can_qk_rmsnorm(const void *q_out, const void *q, int64_t rows_q,
                                   const void *k_out, const void *k, int64_t rows_k,
                                   int64_t Dh, const void *wq, const void *wk,
+                                  float eps, int dtype, uint32_t flags);
+
+/* ------------------------------------------------------------------------
+ * adaln_ln_modulate_fp8
+ *   out[b, n, :] = e4m3(y / qscale),  y = LN(x) * (1 + scale) + shift
+ *
+ * The "flux2_layernorm_modulate_fp8_quant" of the Fused Kernels page
+ * (Quantized layout producers table: LayerNorm plus adaLN modulation
+ * directly into static FP8 output): adaln_ln_modulate followed by a static
+ * per-tensor FP8 quantisation, the 16-bit y never written.
+ *   out     (B, N, D) contiguous bytes, FP8 e4m3 (the finite-only variant:
+ *           largest value 448, 0x7F / 0xFF NaN).
+ *   qscale  DEVICE pointer to one binary32 scale (4-byte aligned), read by
+ *           the kernel after earlier work on the stream; a positive finite
+ *           value is expected (anything else gives what the IEEE division
+ *           gives, then saturation).
+ *   x, scale, shift, eps, dtype: as adaln_ln_modulate.  out overlaps no
+ *           input (no in-place form: the element sizes differ).
+ *   Kernels: the contiguous-rows kernel under its conditions, otherwise
+ *   the general kernel (same bits); the transposed-view tile kernels do not
+ *   write FP8.
+ * Numerics: y exactly as adaln_ln_modulate stores it, then one IEEE
+ * binary32 division by *qscale, round to nearest even to e4m3, saturating
+ * at +-448 (infinities included); NaN stays NaN.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_ln_modulate_fp8(void *out, const void *qscale, const void *x,
+                                  int64_t B, int64_t N, int64_t D,
+                                  int64_t sxB, int64_t sxN, int64_t sxD,
+                                  const void *scale, int64_t s_scale_b,
+                                  const void *shift, int64_t s_shift_b,
+                                  float eps, int dtype, uint32_t flags, void *stream);
+
+adaln_status adaln_can_ln_modulate_fp8(const void *out, const void *qscale, const void *x,
+                                      int64_t B, int64_t N, int64_t D,
+                                      int64_t sxB, int64_t sxN, int64_t sxD,
+                                      const void *scale, int64_t s_scale_b,
+                                      const void *shift, int64_t s_shift_b,
+                                      float eps, int dtype, uint32_t flags);
+
+/* Which kernel adaln_ln_modulate_fp8 would launch (codes of
+ * adaln_ln_modulate_variant), or -status for invalid arguments. */
+int adaln_ln_modulate_fp8_variant(const void *out, const void *qscale, const void *x,
+                                  int64_t B, int64_t N, int64_t D,
+                                  int64_t sxB, int64_t sxN, int64_t sxD,
+                                  const void *scale, int64_t s_scale_b,
+                                  const void *shift, int64_t s_shift_b,
                                   float eps, int dtype, uint32_t flags);
 
 /* ------------------------------------------------------------------------

@@ -206,6 +206,18 @@ def temb_slices(S: int = 32760, K: int = 6, D: int = 3072) -> Workload:
     })
 
 
+def ln_fp8_flux(N: int = 4608, D: int = 3072) -> Workload:
+    """LayerNorm + modulate into static FP8 at a FLUX-like width: 4096 image
+    and 512 text tokens of 3072 channels; static scale 0.03 (outputs span
+    the e4m3 range and a few saturate)."""
+    return Workload(f"ln_modulate_fp8 (1,{N},{D}) static e4m3 output", "ln_modulate_fp8", {
+        "x": TensorSpec((1, N, D), 0.0, 1.0, SEEDS["x"]),
+        "scale": TensorSpec((1, 1, D), 0.0, 0.1, SEEDS["scale"]),
+        "shift": TensorSpec((1, 1, D), 0.0, 0.1, SEEDS["shift"]),
+    }, {"eps": 1e-6, "qscale": 0.03})
+
+
 def all_workloads() -> List[Workload]:
     return [ln_tiny(), ln_sana(), ln_glm(), gate_add_glm(), qk_glm(), gelu_wan("bf16"),
-            gelu_wan("fp16"), rms_rows(), rms_tokens(), gate_rms_tokens(), qk_rms(), temb_slices()]
+            gelu_wan("fp16"), rms_rows(), rms_tokens(), gate_rms_tokens(), qk_rms(), temb_slices(),
+            ln_fp8_flux()]

@@ -216,3 +216,20 @@ def test_temb_table_slices_validation(ad):
     a[10] = 2
     assert f(*a) == 6
     assert f(O, 0, T, 0, E, 1, 2, 3, 1, 8, 0) == 0  # K = 1 ignores the slice stride
+
+
+def test_ln_modulate_fp8_validation(ad):
+    f = ad.capi.adaln_can_ln_modulate_fp8
+    O, Q, X, S, H = 1 << 36, 1 << 37, 1 << 38, 1 << 39, (1 << 39) + 8192
+    B, N, D = 1, 4608, 3072
+    args = lambda o=O, q=Q, x=X, s=S, strides=None, eps=1e-6, dt=0, fl=0: (
+        o, q, x, B, N, D, *(strides or (N * D, D, 1)), s, 0, H, 0, eps, dt, fl)
+    assert f(*args()) == 0
+    assert f(*args(q=0)) == 1
+    assert f(*args(q=Q + 2)) == 4                 # the scale is a 4-byte float
+    assert f(*args(o=X)) == 7                     # no in-place form
+    assert f(*args(o=S - 100)) == 7
+    assert f(*args(o=Q - 8)) == 7                 # out over the scale value
+    assert f(*args(o=O + 1)) == 0                 # byte outputs need no alignment
+    assert f(*args(dt=2)) == 2 and f(*args(eps=-1.0)) == 6 and f(*args(fl=8)) == 6
+    assert f(*args(strides=(N * D, 1, N))) == 0   # any strides (the general kernel)
