@@ -194,7 +194,7 @@ static inline bool ln_aligned(const void *p, int a) { return ((uintptr_t)p % (ui
 static inline bool ln_mult(int64_t v, int64_t a) { return v % a == 0; }
 
 bool ln_rows_ok(const LnArgs &a);
-constexpr int kRowsMaxNI = 8;     // contiguous rows in registers: D <= 4096
+constexpr int kRowsMaxNI = 12;    // contiguous rows in registers: D <= 6144
 constexpr int kTokensMaxNI = 12;  // tokens tile in shared memory: D <= 6144
 // contiguous-rows kernels (ln_rows_*.cu): LayerNorm / RMSNorm, without or
 // with the residual gate (a.gate; x, y, r_out, out contiguous)

@@ -67,8 +67,10 @@ struct RowsParams {
     const float *qscale;
 };
 
+// NI <= 8 (D <= 4096): two CTAs per SM (at most 128 registers a thread);
+// NI 9..12 (D <= 6144): one CTA per SM, the longer row in registers.
 template <DT T, int NI, bool TAIL, bool OPSH, int GM, bool RMS, bool E4M3 = false>
-__global__ void __launch_bounds__(kRowsThreads, 2)
+__global__ void __launch_bounds__(kRowsThreads, NI <= 8 ? 2 : 1)
 ln_rows_kernel(const RowsParams p) {
     constexpr bool GATE = GM != GATE_NONE;
     constexpr bool GTAB = OPSH && GM == GATE_ROW;      // gate rows in the shared table
@@ -361,6 +363,10 @@ static cudaError_t rows_vec(const LnArgs &a, bool pdl, cudaStream_t s, const Dev
         case 6: return rows_tail<T, 6, GM, RMS, E4M3>(a, pdl, s, dev);
         case 7: return rows_tail<T, 7, GM, RMS, E4M3>(a, pdl, s, dev);
         case 8: return rows_tail<T, 8, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 9: return rows_tail<T, 9, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 10: return rows_tail<T, 10, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 11: return rows_tail<T, 11, GM, RMS, E4M3>(a, pdl, s, dev);
+        case 12: return rows_tail<T, 12, GM, RMS, E4M3>(a, pdl, s, dev);
     }
     return cudaErrorInvalidValue;
 }

@@ -277,6 +277,13 @@ def make_workloads(dev, which, n_sets=None, flags=0):
         out["qk_rms"] = ([(lambda t=t: ad.qk_rmsnorm(t[0], t[1], t[2], t[3], 1e-6, q_out=t[4], k_out=t[5],
                                                     flags=flags))
                           for t in copies(base, sets_for(nb))], nb, w.name)
+    if "wan_ln" in which:
+        w = synth.ln_wan()
+        nb = ln_bytes(1, 32760, 5120)
+        base = [torch_bits(w.tensors[k].draw(), "bf16", dev) for k in ("x", "scale", "shift")]
+        base.append(torch.empty_like(base[0]))
+        out["wan_ln"] = ([(lambda x=x, sc=sc, sh=sh, o=o: ad.ln_modulate(x, sc, sh, 1e-6, out=o, flags=flags))
+                          for x, sc, sh, o in copies(base, sets_for(nb))], nb, w.name)
     if "fp8" in which:
         w = synth.ln_fp8_flux()
         N, D = 4608, 3072
@@ -357,6 +364,9 @@ def make_eager(dev, name, nb):
             wq, wk = g((128,), 0.05), g((128,), 0.05)
             out.append(lambda q=q, k=k, wq=wq, wk=wk: (F.rms_norm(q, (128,), wq, 1e-6),
                                                        F.rms_norm(k, (128,), wk, 1e-6)))
+        elif name == "wan_ln":
+            x, sc, sh = g((1, 32760, 5120)), g((1, 1, 5120), 0.1), g((1, 1, 5120), 0.1)
+            out.append(lambda x=x, sc=sc, sh=sh: F.layer_norm(x, (5120,), eps=1e-6) * (1 + sc) + sh)
         elif name == "fp8":
             x, sc, sh = g((1, 4608, 3072)), g((1, 1, 3072), 0.1), g((1, 1, 3072), 0.1)
             out.append(lambda x=x, sc=sc, sh=sh: (F.layer_norm(x, (3072,), eps=1e-6) * (1 + sc) + sh).float()
@@ -726,7 +736,7 @@ def run_ours(args):
                        "one_stream_ms_per_step": round(serial_ms, 4)}
     if rank == 0 and not args.no_per_config:
         names = ["tiny", "sana", "sana_nmod2", "glm_ln", "glm_gate", "glm_gate_ln", "qk", "gelu_bf16",
-                 "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms", "temb", "fp8"]
+                 "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms", "temb", "fp8", "wan_ln"]
         per = {}
         steps = max(20, min(args.steps, 400))
         for name in names:
@@ -777,7 +787,7 @@ def main():
     p.add_argument("--quick", action="store_true", help="headline only (for profiler runs)")
     p.add_argument("--only", default="sana",
                    choices=["sana", "sana_nmod2", "tiny", "glm_ln", "glm_gate", "glm_gate_ln", "qk",
-                            "gelu_bf16", "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms", "temb", "fp8"],
+                            "gelu_bf16", "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms", "temb", "fp8", "wan_ln"],
                    help="workload timed as the headline (profiling runs); the JSON line's metric "
                         "and roofline describe the Sana LN+modulate only when this is 'sana'")
     args = p.parse_args()

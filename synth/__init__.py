@@ -217,7 +217,17 @@ def ln_fp8_flux(N: int = 4608, D: int = 3072) -> Workload:
     }, {"eps": 1e-6, "qscale": 0.03})
 
 
+def ln_wan(N: int = 32760, D: int = 5120) -> Workload:
+    """LayerNorm + modulate on 5120-wide rows (the Wan FFN workload's
+    tokens at the model width), one scale / shift row per sample."""
+    return Workload(f"ln_modulate (1,{N},{D}) per-sample rows", "ln_modulate", {
+        "x": TensorSpec((1, N, D), 0.0, 1.0, SEEDS["x"]),
+        "scale": TensorSpec((1, 1, D), 0.0, 0.1, SEEDS["scale"]),
+        "shift": TensorSpec((1, 1, D), 0.0, 0.1, SEEDS["shift"]),
+    }, {"eps": 1e-6})
+
+
 def all_workloads() -> List[Workload]:
     return [ln_tiny(), ln_sana(), ln_glm(), gate_add_glm(), qk_glm(), gelu_wan("bf16"),
             gelu_wan("fp16"), rms_rows(), rms_tokens(), gate_rms_tokens(), qk_rms(), temb_slices(),
-            ln_fp8_flux()]
+            ln_fp8_flux(), ln_wan()]

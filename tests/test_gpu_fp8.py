@@ -67,9 +67,9 @@ def test_scales_in_range_and_saturating(ad, qscale):
         assert ((ref & 0x7F) == 0x7E).any()   # saturated codes present
 
 
-@pytest.mark.parametrize("D", [5120, 8192])
-def test_general_kernel_large_d(ad, D):
-    case(ad, 2, 11, D, 0.02, seed=D + 1, expect="generic")
+@pytest.mark.parametrize("D,expect", [(5120, "rows"), (6144, "rows"), (8192, "generic")])
+def test_large_d(ad, D, expect):
+    case(ad, 2, 11, D, 0.02, seed=D + 1, expect=expect)
 
 
 def test_transposed_view_takes_the_general_kernel(ad):

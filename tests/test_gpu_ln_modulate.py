@@ -183,12 +183,16 @@ def test_generic_path(ad, D, dtype):
     assert_bits_equal(got, ref, dtype, f"generic D={D}")
 
 
-def test_large_contiguous_goes_generic(ad):
-    B, N, D = 1, 33, 5120
-    x = synth.normal_bits(3, B * N * D, 0, 1).reshape(B, N, D)
-    table = synth.normal_bits(4, 2 * D, 0, 0.1).reshape(1, 2, D)
-    got, ref = run_both(ad, x, B, N, D, (N * D, D, 1), table, D, 0, 2 * D, 1e-6, expect="generic")
-    assert_bits_equal(got, ref, what="D=5120")
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("D,expect", [(4100, "rows"), (4608, "rows"), (5120, "rows"), (5632, "rows"),
+                                      (6140, "rows"), (6144, "rows"), (6148, "generic")])
+def test_large_contiguous_rows(ad, D, expect, dtype):
+    # one CTA per SM holds rows of up to 6144 elements; past that the general kernel
+    B, N = 2, 33
+    x = synth.normal_bits(D + 3, B * N * D, 0, 1, dtype).reshape(B, N, D)
+    table = synth.normal_bits(D + 4, B * 2 * D, 0, 0.1, dtype).reshape(B, 2, D)
+    got, ref = run_both(ad, x, B, N, D, (N * D, D, 1), table, D, 0, 2 * D, 1e-6, dtype, expect=expect)
+    assert_bits_equal(got, ref, dtype, what=f"D={D}")
 
 
 # ------------------------------------------------------------ edge cases

@@ -93,9 +93,9 @@ def test_rms_rows_kernel(ad, D, dtype):
     case(ad, "rms", 3, 37, D, dtype, seed=D, expect="rows")
 
 
-@pytest.mark.parametrize("D", [4100, 5120, 8192])
-def test_rms_general_kernel_large_d(ad, D):
-    case(ad, "rms", 2, 19, D, seed=D + 1, expect="generic")
+@pytest.mark.parametrize("D", [4100, 5120, 6144, 8192])
+def test_rms_large_d(ad, D):
+    case(ad, "rms", 2, 19, D, seed=D + 1, expect="rows" if D <= 6144 else "generic")
 
 
 def test_rms_transposed_view_takes_the_general_kernel(ad):
@@ -105,15 +105,15 @@ def test_rms_transposed_view_takes_the_general_kernel(ad):
 @pytest.mark.parametrize("norm", ["layer", "rms"])
 @pytest.mark.parametrize("D", [516, 3072, 5120])
 def test_per_token_modulation_rows(ad, norm, D):
-    case(ad, norm, 2, 33, D, seed=D + 7, per_token=True, expect="rows" if D <= 4096 else "generic")
+    case(ad, norm, 2, 33, D, seed=D + 7, per_token=True, expect="rows" if D <= 6144 else "generic")
 
 
 @pytest.mark.parametrize("norm", ["layer", "rms"])
 @pytest.mark.parametrize("gate", ["sample", "token", "scalar"])
-@pytest.mark.parametrize("D", [12, 2240, 4096, 5120])
+@pytest.mark.parametrize("D", [12, 2240, 4096, 5120, 8192])
 def test_gated(ad, norm, gate, D):
     case(ad, norm, 2, 21, D, seed=D + 11, gate=gate, per_token=(gate == "token"),
-         expect="rows" if D <= 4096 else "generic")
+         expect="rows" if D <= 6144 else "generic")
 
 
 @pytest.mark.parametrize("norm", ["layer", "rms"])
@@ -126,7 +126,8 @@ def test_gated_per_sample_modulation_with_per_token_gates(ad, norm):
 @pytest.mark.parametrize("in_place", ["x", "y"])
 def test_gated_in_place(ad, in_place):
     case(ad, "rms", 2, 25, 2048, seed=31, gate="scalar", per_token=True, in_place=in_place, expect="rows")
-    case(ad, "layer", 2, 25, 5120, seed=32, gate="token", per_token=True, in_place=in_place, expect="generic")
+    case(ad, "layer", 2, 25, 5120, seed=32, gate="token", per_token=True, in_place=in_place, expect="rows")
+    case(ad, "layer", 2, 25, 8192, seed=33, gate="token", per_token=True, in_place=in_place, expect="generic")
 
 
 @pytest.mark.parametrize("B,D", [(2, 2728), (2, 2732), (4, 1364), (8, 1024)])

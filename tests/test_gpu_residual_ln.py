@@ -45,9 +45,9 @@ def test_fused_kernel_shapes(ad, D, dtype):
     case(ad, 3, 37, D, dtype, seed=D)
 
 
-@pytest.mark.parametrize("D", [4100, 5120, 8192])
-def test_two_launch_path(ad, D):
-    # past the rows kernel's D: gate-add then LN+modulate, the same bits
+@pytest.mark.parametrize("D", [4100, 5120, 6144, 8192])
+def test_large_d(ad, D):
+    # rows of up to 6144 in registers (one CTA per SM); past that the general kernel
     case(ad, 2, 19, D, seed=D + 1)
 
 
