@@ -187,7 +187,7 @@ __device__ __forceinline__ float div_by_recip(float a, float b, float r) {
 // kernel turns that into a window [lo, hi] of 16-bit magnitude patterns
 // (|y| >= max(2^-100, 2^-99 / |qr|), |y| <= min(2^100, 2^99 / |qr|): a
 // factor 2 of margin for the product's rounding), checks a chunk's 4
-// patterns against it with two packed min / max and two packed compares,
+// magnitudes against it with one packed min, one max and two compares,
 // runs the correction on f32x2 pairs when they all fit, and takes the exact
 // quotient one value at a time (zeros, NaN, extreme magnitudes) otherwise.
 struct QuantE4M3 {
@@ -233,13 +233,28 @@ static __device__ __noinline__ float4 quant_exact4(float4 a, float qs, float qr)
                        div_by_recip(a.w, qs, qr));
 }
 
+// every |value| of the two packed pairs lies in [lo, hi] (lo2 / hi2: the
+// bounds' patterns in both halves); the storage type's own packed min / max
+// and compares, on magnitudes (a NaN may pass: its quotient is NaN either way)
+template <DT T> __device__ __forceinline__ bool window4(uint32_t m0, uint32_t m1, uint32_t lo2, uint32_t hi2);
+template <> __device__ __forceinline__ bool window4<DT::BF16>(uint32_t m0, uint32_t m1, uint32_t lo2, uint32_t hi2) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&m0);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&m1);
+    return __hble2(__hmax2(a, b), *reinterpret_cast<const __nv_bfloat162 *>(&hi2)) &&
+           __hbge2(__hmin2(a, b), *reinterpret_cast<const __nv_bfloat162 *>(&lo2));
+}
+template <> __device__ __forceinline__ bool window4<DT::FP16>(uint32_t m0, uint32_t m1, uint32_t lo2, uint32_t hi2) {
+    const __half2 a = *reinterpret_cast<const __half2 *>(&m0);
+    const __half2 b = *reinterpret_cast<const __half2 *>(&m1);
+    return __hble2(__hmax2(a, b), *reinterpret_cast<const __half2 *>(&hi2)) &&
+           __hbge2(__hmin2(a, b), *reinterpret_cast<const __half2 *>(&lo2));
+}
+
 // the e4m3 codes of 4 storage values (2 packed pairs), in memory order
 template <DT T>
 __device__ __forceinline__ uint32_t quant4_e4m3(const uint32_t *o, const QuantE4M3 &c) {
-    const uint32_t m0 = o[0] & 0x7fff7fffu, m1 = o[1] & 0x7fff7fffu;
-    const uint32_t inside = __vcmpleu2(__vmaxu2(m0, m1), c.hi2) & __vcmpgeu2(__vminu2(m0, m1), c.lo2);
     float q0, q1, q2, q3;
-    if (inside == 0xffffffffu) {
+    if (window4<T>(o[0] & 0x7fff7fffu, o[1] & 0x7fff7fffu, c.lo2, c.hi2)) {
         const f2_t a01 = f2(lo_f32<T>(o[0]), hi_f32<T>(o[0])), a23 = f2(lo_f32<T>(o[1]), hi_f32<T>(o[1]));
         const f2_t r2 = f2(c.qr, c.qr), nb2 = f2(c.nqs, c.nqs);
         f2_t p01 = f2_mul(a01, r2), p23 = f2_mul(a23, r2);
