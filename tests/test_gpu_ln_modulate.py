@@ -138,9 +138,27 @@ def test_tokens_tiles_many_per_cta(ad, B, N, D, dtype):
     assert ad.tma_wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("B,N,D", [(2, 1024, 2240),   # the headline: 128 tiles, one per CTA
+                                   (1, 1000, 2240),   # ragged last tile (8 of 16 tokens)
+                                   (2, 40, 516),      # tail chunk, few tiles
+                                   (2, 2600, 1024),   # 326 tiles: two or three per CTA
+                                   (3, 1624, 512),    # ragged last tile of each sample
+                                   (1, 8, 5120)])     # one half tile of the largest D
+def test_tma_tile_shapes(ad, B, N, D, dtype):
+    # the path needs N % 8 == 0 (16-byte d-row strides for the tensor map)
+    x = synth.normal_bits(N + D, B * D * N, 0.1, 1.2, dtype).reshape(B, D, N)
+    table = synth.normal_bits(N + D + 1, B * 6 * D, 0, 0.1, dtype).reshape(B, 6, D)
+    rows = range(0, B * N, 5) if B * N > 3000 else None
+    got, ref = run_both(ad, x, B, N, D, (D * N, 1, N), table, D, 0, 6 * D, 1e-6, dtype,
+                        expect="tokens_tma", rows=rows)
+    assert_bits_equal(got, ref, dtype, f"tma tiles B={B} N={N} D={D}")
+    assert ad.tma_wait_timeouts() == 0
+
+
 def test_sana_takes_the_tma_tile_kernel(ad):
-    # the transposed headline shape goes through the 16-token TMA tiles; the
-    # largest D past them through the cp.async tiles
+    # the transposed headline shape goes through the TMA tiles; the largest
+    # D past them through the cp.async tiles
     B, N, D = 2, 1024, 2240
     x = synth.normal_bits(35, B * D * N, 0, 1).reshape(B, D, N)
     table = synth.normal_bits(36, B * 6 * D, 0, 0.1).reshape(B, 6, D)
