@@ -4,6 +4,7 @@
 // logical lane's vec4 chunk), so rows only need 8-byte aligned starts.
 #pragma once
 #include "ln_common.cuh"
+#include "quant_e4m3.cuh"
 
 namespace adaln {
 

@@ -4,7 +4,7 @@
 // kernel's 4-wide e4m3 quantiser on arrays of 16-bit storage values.
 #include <cuda_runtime.h>
 
-#include "../../adaln_modulate_gb300/csrc/common.cuh"
+#include "../../adaln_modulate_gb300/csrc/quant_e4m3.cuh"
 
 __global__ void div_sweep_kernel(const float *a, float b, float *mine, float *ieee, long long n) {
     const float r = __frcp_rn(b);
