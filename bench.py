@@ -542,6 +542,18 @@ def copy_calls(dev, nbytes):
     return [(lambda a=a, b=b: torch.mul(a, 1, out=b)) for a, b in bufs]
 
 
+def memcpy_calls(dev, nbytes):
+    """Same-byte device-to-device copies through cudaMemcpyAsync (torch's
+    copy_ of contiguous tensors of one dtype), rotating like the ops."""
+    import torch
+    n = nbytes // 2 // 2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sets = max(1, min(MAX_SETS, -(-4 * l2 // nbytes)))
+    bufs = [(torch.ones(n, dtype=torch.bfloat16, device=dev), torch.empty(n, dtype=torch.bfloat16, device=dev))
+            for _ in range(sets)]
+    return [(lambda a=a, b=b: b.copy_(a)) for a, b in bufs]
+
+
 # ------------------------------------------------------------ CPU baseline
 
 def cpu_model():
@@ -742,16 +754,22 @@ def run_ours(args):
         for name in names:
             wl = make_workloads(dev, [name], flags=ad.FLAG_PDL)
             cl, nb, desc = wl[name]
-            ms = time_block(cl, steps, 3)
+            # five block-timed repetitions: the per-call median and spread
+            reps = sorted(time_block(cl, max(10, steps // 5), 3) for _ in range(5))
+            ms = statistics.median(reps)
             iso = time_calls(cl[0], max(10, min(args.steps, 200)), 5, flush)
             cc = copy_calls(dev, nb)
             msc = time_block(cc, steps, 3)
             del cc
+            mc = memcpy_calls(dev, nb)
+            msm = time_block(mc, max(10, steps // 4), 3)
+            del mc
             ec = make_eager(dev, name, nb)
             mse = time_block(ec, min(steps, 100), 3)
             del ec
             us, usc = ms * 1e3, msc * 1e3
             per[name] = {"workload": desc, "us_per_call": round(us, 3),
+                         "us_per_call_p10_p90": [round(reps[0] * 1e3, 3), round(reps[-1] * 1e3, 3)],
                          "gbs": round(nb / (us * 1e-6) / 1e9, 1),
                          "frac_of_hbm_peak": round(nb / (us * 1e-6) / 1e9 / hbm, 4),
                          "algorithmic_bytes": nb, "rotating_sets": len(cl),
@@ -759,13 +777,16 @@ def run_ours(args):
                          "isolated_call_us_median": round(statistics.median(iso) * 1e3, 3),
                          "copy_same_bytes_us": round(usc, 3),
                          "copy_same_bytes_gbs": round(nb / (usc * 1e-6) / 1e9, 1),
+                         "memcpy_d2d_same_bytes_us": round(msm * 1e3, 3),
                          "torch_eager_us": round(mse * 1e3, 3)}
             del wl, cl
             torch.cuda.empty_cache()
         line["per_config"] = per
         line["per_config_how"] = ("each workload timed like the headline (rotating sets >= 4x L2, CUDA "
-                                  "graphs, PDL) next to a same-byte SM copy and the torch eager chain the "
-                                  "op replaces (context only), timed the same way")
+                                  "graphs, PDL): the median of five block-timed repetitions (the extremes "
+                                  "of the five as p10 / p90), next to a same-byte SM copy, a same-byte "
+                                  "device-to-device cudaMemcpyAsync and the torch eager chain the op "
+                                  "replaces (context only), timed the same way")
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
