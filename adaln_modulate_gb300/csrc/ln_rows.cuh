@@ -117,9 +117,8 @@ ln_rows_kernel(const RowsParams p) {
 
     // xv[i][s] = the 4 elements of lane l0 + 8s at step i (2 registers)
     uint32_t xv[NI][4][2];
-    auto load_row = [&](int64_t row) {
-        const int64_t b = row / N;
-        const uint16_t *xr = p.x + b * p.sxB + (row - b * N) * p.sxN + c0;
+    auto load_row = [&](int64_t b, int64_t n) {
+        const uint16_t *xr = p.x + b * p.sxB + n * p.sxN + c0;
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
 #pragma unroll
@@ -132,8 +131,19 @@ ln_rows_kernel(const RowsParams p) {
             }
         }
     };
+    // (b, n) of the warp's row, advanced with the row (a division only when
+    // the warp's next row lies in a later sample)
     int64_t row = r0 + warp;
-    if (row < r1) load_row(row);
+    int64_t rb = row / N, rn = row - rb * N;
+    auto next_bn = [&](int64_t &b, int64_t &n) {
+        n += kRowsThreads / 32;
+        if (n >= N) {
+            const int64_t q = n / N;
+            b += q;
+            n -= q * N;
+        }
+    };
+    if (row < r1) load_row(rb, rn);
 
     if constexpr (OPSH) {
         // all loads of a batch in flight before any is used
@@ -145,7 +155,7 @@ ln_rows_kernel(const RowsParams p) {
             for (int k = 0; k < kFill; ++k) {
                 const int e = base + k * kRowsThreads + threadIdx.x;
                 if (e < npairs) {
-                    const int bb = e / half, cp = e - bb * half;
+                    const int bb = p.B == 1 ? 0 : e / half, cp = e - bb * half;
                     asm("ld.global.nc.b32 %0, [%1];" : "=r"(s2[k]) : "l"(p.scale + bb * p.s_scale_b + 2 * cp));
                     asm("ld.global.nc.b32 %0, [%1];" : "=r"(h2[k]) : "l"(p.shift + bb * p.s_shift_b + 2 * cp));
                     if constexpr (GTAB)
@@ -166,7 +176,9 @@ ln_rows_kernel(const RowsParams p) {
     }
 
     for (; row < r1; row += kRowsThreads / 32) {
-        const int64_t b = row / N, n = row - b * N;
+        const int64_t b = rb, n = rn;
+        int64_t bn = rb, nn = rn;  // the warp's next row
+        next_bn(bn, nn);
 
         // pass 1: Welford (or the sum of squares) of lanes (s0, s1) and
         // (s2, s3), one f32x2 op each
@@ -249,10 +261,7 @@ ln_rows_kernel(const RowsParams p) {
 
         // this row has arrived: ask L2 for the warp's next row now, so that
         // its DRAM reads overlap this row's fold, output pass and stores
-        if (u == 0 && row + kRowsThreads / 32 < r1) {
-            const int64_t rn = row + kRowsThreads / 32, bn = rn / N;
-            prefetch_l2(p.x + bn * p.sxB + (rn - bn * N) * p.sxN, (uint64_t)D * 2);
-        }
+        if (u == 0 && row + kRowsThreads / 32 < r1) prefetch_l2(p.x + bn * p.sxB + nn * p.sxN, (uint64_t)D * 2);
 
         float mean, m2;
         if constexpr (RMS) {
@@ -306,7 +315,9 @@ ln_rows_kernel(const RowsParams p) {
                 }
             }
         }
-        if (row + kRowsThreads / 32 < r1) load_row(row + kRowsThreads / 32);
+        if (row + kRowsThreads / 32 < r1) load_row(bn, nn);
+        rb = bn;
+        rn = nn;
     }
 }
 
