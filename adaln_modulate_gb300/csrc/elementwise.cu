@@ -49,10 +49,13 @@ gate_add_kernel(uint16_t *out, const uint16_t *x, const uint16_t *gate, int64_t 
     pdl_trigger();
     constexpr int R = EPT / 2;
     const int64_t stride = (int64_t)gridDim.x * kEwThreads;
-    for (int64_t v = (int64_t)blockIdx.x * kEwThreads + threadIdx.x; v < nvec; v += stride) {
+    // sample b and column col of the thread's element, advanced by the
+    // grid step with a carry (no division per iteration)
+    const int64_t v0 = (int64_t)blockIdx.x * kEwThreads + threadIdx.x, step = stride * EPT;
+    const int64_t qb = step / ND, rb = step - qb * ND, rc = step % D;
+    int64_t b = v0 * EPT / ND, in_b = v0 * EPT - b * ND, col = v0 * EPT % D;
+    for (int64_t v = v0; v < nvec; v += stride) {
         const int64_t e0 = v * EPT;
-        const int64_t b = e0 / ND;
-        const int64_t col = (e0 - b * ND) % D;
         uint32_t xr[R], yr[R], gr[R], o[R];
         Acc<EPT>::ld_s(xr, x + e0);
         Acc<EPT>::ld_s(yr, y + e0);
@@ -60,6 +63,14 @@ gate_add_kernel(uint16_t *out, const uint16_t *x, const uint16_t *gate, int64_t 
 #pragma unroll
         for (int k = 0; k < R; ++k) o[k] = add16x2<T>(xr[k], mul16x2<T>(gr[k], yr[k]));
         Acc<EPT>::st(out + e0, o);
+        b += qb;
+        in_b += rb;
+        if (in_b >= ND) {
+            in_b -= ND;
+            ++b;
+        }
+        col += rc;
+        if (col >= D) col -= D;
     }
 }
 
@@ -71,9 +82,15 @@ gate_add_scalar_kernel(uint16_t *out, const uint16_t *x, const uint16_t *gate, i
     pdl_wait();
     pdl_trigger();
     const int64_t stride = (int64_t)gridDim.x * kEwThreads;
-    for (int64_t e = (int64_t)blockIdx.x * kEwThreads + threadIdx.x; e < n; e += stride) {
-        const int64_t b = e / ND;
-        const int64_t col = (e - b * ND) % D;
+    const int64_t e_0 = (int64_t)blockIdx.x * kEwThreads + threadIdx.x;
+    const int64_t qb = stride / ND, rb = stride - qb * ND, rc = stride % D;
+    int64_t b = e_0 / ND, in_b = e_0 - b * ND, col = e_0 % D;
+    for (int64_t e = e_0; e < n; e += stride, b += qb, in_b += rb, col += rc) {
+        if (in_b >= ND) {
+            in_b -= ND;
+            ++b;
+        }
+        if (col >= D) col -= D;
         const float gy = h_f32<T>(to16_rn<T>(__fmul_rn(h_f32<T>(gate[b * s_gate_b + col]), h_f32<T>(y[e]))));
         out[e] = to16_rn<T>(__fadd_rn(h_f32<T>(x[e]), gy));
     }

@@ -61,9 +61,16 @@ temb_slices_kernel(float *__restrict__ out, int64_t s_out_k, const void *__restr
     const int64_t W = VEC ? D / 8 : D;  // units per (token, chunk) row
     const int64_t total = BS * K * W;
     const int64_t stride = (int64_t)gridDim.x * kTembThreads;
-    for (int64_t u = (int64_t)blockIdx.x * kTembThreads + threadIdx.x; u < total; u += stride) {
-        const int64_t row = u / W, w = u - row * W;  // row = bs * K + k: temb storage order
-        const int64_t bs = row / K, k = row - bs * K;
+    // unit u = (bs * K + k) * W + w (temb storage order): (bs, k, w) advanced
+    // by the grid step with carries, no division per iteration
+    const int64_t u0 = (int64_t)blockIdx.x * kTembThreads + threadIdx.x;
+    const int64_t qr = stride / W, rw = stride - qr * W;      // rows and units of one step
+    const int64_t qs0 = qr / K, rk0 = qr - qs0 * K;           // a step of qr rows
+    const int64_t qs1 = (qr + 1) / K, rk1 = (qr + 1) - qs1 * K;  // a step of qr + 1 rows
+    int64_t row0 = u0 / W, w = u0 - row0 * W;
+    int64_t bs = row0 / K, k = row0 - bs * K;
+    for (int64_t u = u0; u < total; u += stride) {
+        const int64_t row = bs * K + k;
         if constexpr (VEC) {
             const int64_t d = 8 * w;
             float e[8], t[8];
@@ -75,6 +82,15 @@ temb_slices_kernel(float *__restrict__ out, int64_t s_out_k, const void *__restr
             st32(out + k * s_out_k + bs * D + d, o);
         } else {
             out[k * s_out_k + bs * D + w] = __fadd_rn(load1_f32<TDT>(table, k * D + w), load1_f32<EDT>(temb, row * D + w));
+        }
+        w += rw;
+        const bool carry = w >= W;
+        if (carry) w -= W;
+        bs += carry ? qs1 : qs0;
+        k += carry ? rk1 : rk0;
+        if (k >= K) {
+            k -= K;
+            ++bs;
         }
     }
 }
