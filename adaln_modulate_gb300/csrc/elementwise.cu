@@ -14,6 +14,8 @@
 // One add or multiply of two storage values done by the packed 16-bit
 // instructions equals binary32 arithmetic followed by one storage rounding
 // (see add16x2 in common.cuh), which is what the chains specify.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -236,12 +238,12 @@ static cudaError_t run_gelu(const GeluArgs &a, bool pdl, cudaStream_t s, const D
                         (const uint16_t *)a.table);
     } else {
         auto k = bias_gelu_kernel<T, EPT>;
-        static bool attr_set[64] = {};  // per device
+        static std::atomic<bool> attr_set[64] = {};  // per device; setting it twice is harmless
         if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-        if (!attr_set[dev.device]) {
+        if (!attr_set[dev.device].load(std::memory_order_acquire)) {
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGeluSmem);
             if (e != cudaSuccess) return e;
-            attr_set[dev.device] = true;
+            attr_set[dev.device].store(true, std::memory_order_release);
         }
         const int64_t nvec = n / EPT;
         const int64_t grid = imin64((nvec + kGeluThreads - 1) / kGeluThreads,

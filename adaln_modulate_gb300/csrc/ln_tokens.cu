@@ -1,5 +1,7 @@
 // ln_modulate kernels for the transposed view (tokens contiguous) and for
 // arbitrary strides.
+#include <atomic>
+
 #include "ln_common.cuh"
 
 namespace adaln {
@@ -190,12 +192,12 @@ template <DT T, int NI>
 static cudaError_t run_tokens(const LnArgs &a, bool pdl, cudaStream_t s, const DeviceInfo &dev) {
     auto k = ln_tokens_kernel<T, NI>;
     const size_t smem = (size_t)NI * 4 * 128 * sizeof(uint4);  // + 8.1 KB static
-    static bool attr_done[64] = {};  // per device, for this (dtype, NI)
+    static std::atomic<bool> attr_done[64] = {};  // per device, for this (dtype, NI); setting it twice is harmless
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-    if (!attr_done[dev.device]) {
+    if (!attr_done[dev.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_done[dev.device] = true;
+        attr_done[dev.device].store(true, std::memory_order_release);
     }
     const int64_t tiles_per_b = (a.N + kTok - 1) / kTok;
     const int64_t ntiles = a.B * tiles_per_b;

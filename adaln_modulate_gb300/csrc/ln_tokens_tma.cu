@@ -22,6 +22,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/adaln.h"
@@ -301,13 +302,13 @@ cudaError_t run_tokens_tma(const LnArgs &a, const CUtensorMap &map, bool pdl, cu
                            const DeviceInfo &dev) {
     auto k = ln_tokens_tma_kernel<T, NI>;
     const size_t smem = tma_dyn_smem(a.D);
-    static bool attr_done[64] = {};
+    static std::atomic<bool> attr_done[64] = {};  // per device; setting it twice is harmless
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-    if (!attr_done[dev.device]) {
+    if (!attr_done[dev.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)tma_dyn_smem(NI * 512));
         if (e != cudaSuccess) return e;
-        attr_done[dev.device] = true;
+        attr_done[dev.device].store(true, std::memory_order_release);
     }
     const int64_t tiles_per_b = (a.N + kTT - 1) / kTT;
     const int64_t ntiles = a.B * tiles_per_b;
