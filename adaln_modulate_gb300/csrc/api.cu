@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <initializer_list>
 #include <mutex>
 
 #include "../../include/adaln.h"
@@ -84,6 +85,15 @@ adaln_status build_tables_locked(int dev) {
 }
 
 bool finite_nonneg(float v) { return isfinite(v) && v >= 0.0f; }
+
+// strides beyond 2^46 elements describe no real buffer and would overflow the
+// byte extents the overlap checks compute
+constexpr int64_t kMaxStride = (int64_t)1 << 46;
+bool strides_ok(std::initializer_list<int64_t> ss) {
+    for (int64_t v : ss)
+        if (v < 0 || v > kMaxStride) return false;
+    return true;
+}
 bool al2(const void *p) { return ((uintptr_t)p & 1u) == 0; }
 bool al8(const void *p) { return ((uintptr_t)p & 7u) == 0; }
 
@@ -103,7 +113,7 @@ adaln_status check_ln(const void *out, const void *x, int64_t B, int64_t N, int6
     if (!out || !x || !scale || !shift) return ADALN_E_NULL;
     if (B < 1 || N < 1 || D < 4 || D > 65536 || D % 4 != 0) return ADALN_E_SHAPE;
     if (B > ((int64_t)1 << 40) / N || B * N > ((int64_t)1 << 46) / D) return ADALN_E_SHAPE;
-    if (sxB < 0 || sxN < 0 || sxD < 0 || s_scale_b < 0 || s_shift_b < 0) return ADALN_E_STRIDE;
+    if (!strides_ok({sxB, sxN, sxD, s_scale_b, s_shift_b})) return ADALN_E_STRIDE;
     if (!finite_nonneg(eps)) return ADALN_E_VALUE;
     if (!al2(out) || !al2(x) || !al2(scale) || !al2(shift)) return ADALN_E_ALIGN;
     const int64_t out_bytes = 2 * B * N * D;
@@ -155,7 +165,7 @@ adaln_status check_gate(const void *out, const void *x, const void *gate, int64_
     if (!out || !x || !gate || !y) return ADALN_E_NULL;
     if (B < 1 || N < 1 || D < 1) return ADALN_E_SHAPE;
     if (B > ((int64_t)1 << 40) / N || B * N > ((int64_t)1 << 46) / D) return ADALN_E_SHAPE;
-    if (s_gate_b < 0) return ADALN_E_STRIDE;
+    if (!strides_ok({s_gate_b})) return ADALN_E_STRIDE;
     if (!al2(out) || !al2(x) || !al2(gate) || !al2(y)) return ADALN_E_ALIGN;
     const int64_t nb = 2 * B * N * D;
     if (overlap(out, nb, x, nb) && out != x) return ADALN_E_OVERLAP;
@@ -203,8 +213,7 @@ adaln_status check_norm(int norm, const void *r_out, const void *out, const void
     if (gate && (!y || !r_out)) return ADALN_E_NULL;
     if (B < 1 || N < 1 || D < 4 || D > 65536 || D % 4 != 0) return ADALN_E_SHAPE;
     if (B > ((int64_t)1 << 40) / N || B * N > ((int64_t)1 << 46) / D) return ADALN_E_SHAPE;
-    if (sxB < 0 || sxN < 0 || sxD < 0 || s_scale_b < 0 || s_scale_n < 0 || s_shift_b < 0 || s_shift_n < 0)
-        return ADALN_E_STRIDE;
+    if (!strides_ok({sxB, sxN, sxD, s_scale_b, s_scale_n, s_shift_b, s_shift_n})) return ADALN_E_STRIDE;
     if (!finite_nonneg(eps)) return ADALN_E_VALUE;
     if (!al2(out) || !al2(x) || !al2(scale) || !al2(shift)) return ADALN_E_ALIGN;
     const int64_t nb = 2 * B * N * D;
@@ -217,7 +226,7 @@ adaln_status check_norm(int norm, const void *r_out, const void *out, const void
         if (overlap(out, nb, x, x_bytes) && !(out == x && x_contig)) return ADALN_E_OVERLAP;
         return ADALN_OK;
     }
-    if (s_gate_b < 0 || s_gate_n < 0 || (s_gate_d != 0 && s_gate_d != 1)) return ADALN_E_STRIDE;
+    if (!strides_ok({s_gate_b, s_gate_n}) || (s_gate_d != 0 && s_gate_d != 1)) return ADALN_E_STRIDE;
     if (!x_contig) return ADALN_E_STRIDE;
     if (!al2(gate) || !al2(y) || !al2(r_out)) return ADALN_E_ALIGN;
     const int64_t g_bytes = extent(B, N, D, s_gate_b, s_gate_n, s_gate_d);
@@ -260,7 +269,7 @@ adaln_status check_ln_fp8(const void *out, const void *qscale, const void *x, in
     if (!out || !qscale || !x || !scale || !shift) return ADALN_E_NULL;
     if (B < 1 || N < 1 || D < 4 || D > 65536 || D % 4 != 0) return ADALN_E_SHAPE;
     if (B > ((int64_t)1 << 40) / N || B * N > ((int64_t)1 << 46) / D) return ADALN_E_SHAPE;
-    if (sxB < 0 || sxN < 0 || sxD < 0 || s_scale_b < 0 || s_shift_b < 0) return ADALN_E_STRIDE;
+    if (!strides_ok({sxB, sxN, sxD, s_scale_b, s_shift_b})) return ADALN_E_STRIDE;
     if (!finite_nonneg(eps)) return ADALN_E_VALUE;
     if (!al2(x) || !al2(scale) || !al2(shift) || ((uintptr_t)qscale & 3u)) return ADALN_E_ALIGN;
     const int64_t nb = B * N * D;

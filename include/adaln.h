@@ -54,7 +54,7 @@ typedef enum adaln_status {
     ADALN_E_DTYPE = 2,   /* dtype is not ADALN_BF16 / ADALN_FP16 */
     ADALN_E_SHAPE = 3,   /* a size is out of range (see each operation) */
     ADALN_E_ALIGN = 4,   /* a pointer is not aligned to the element size */
-    ADALN_E_STRIDE = 5,  /* a stride is negative or makes rows overlap */
+    ADALN_E_STRIDE = 5,  /* a stride is negative, above 2^46 elements, or not allowed */
     ADALN_E_VALUE = 6,   /* eps negative or not finite, or unknown flag bits */
     ADALN_E_OVERLAP = 7, /* an output overlaps an input in a way not allowed */
     ADALN_E_CUDA = 8     /* a CUDA runtime call failed */

@@ -233,3 +233,14 @@ def test_ln_modulate_fp8_validation(ad):
     assert f(*args(o=O + 1)) == 0                 # byte outputs need no alignment
     assert f(*args(dt=2)) == 2 and f(*args(eps=-1.0)) == 6 and f(*args(fl=8)) == 6
     assert f(*args(strides=(N * D, 1, N))) == 0   # any strides (the general kernel)
+
+
+def test_huge_strides_are_refused(ad):
+    # a stride past 2^46 elements would overflow the byte extents of the overlap checks
+    big = 1 << 50
+    assert ln_can(ad, strides=(big, 2240, 1)) == 5
+    assert ln_can(ad, ssb=big) == 5
+    f = ad.capi.adaln_can_norm_scale_shift
+    assert f(0, 0, OUT, X, 2, 16, 2240, 16 * 2240, 2240, 1, 0, 0, 0, 1, 0, SC, 6 * 2240, big, SH, 6 * 2240, 0,
+             1e-6, 0, 0) == 5
+    assert ad.capi.adaln_can_residual_gate_add(OUT, X, SC, big, X + (1 << 30), 2, 16, 2240, 0, 0) == 5
