@@ -30,7 +30,8 @@ def assert_codes_equal(got, ref, what=""):
     assert not bad.any(), f"{what}: {int(bad.sum())} of {got.size} codes differ, first at {np.argmax(bad)}"
 
 
-def case(ad, B, N, D, qscale, dtype="bf16", seed=0, layout="rows", expect=None, rows=None, x_bits=None):
+def case(ad, B, N, D, qscale, dtype="bf16", seed=0, layout="rows", expect=None, rows=None, x_bits=None,
+         tab_bits=None):
     if layout == "tokens":
         xb = synth.normal_bits(seed, B * D * N, 0.2, 1, dtype) if x_bits is None else x_bits
         strides = (D * N, 1, N)
@@ -39,7 +40,7 @@ def case(ad, B, N, D, qscale, dtype="bf16", seed=0, layout="rows", expect=None, 
         xb = synth.normal_bits(seed, B * N * D, 0.2, 1, dtype) if x_bits is None else x_bits
         strides = (N * D, D, 1)
         x = dev_tensor(xb, dtype).view(B, N, D)
-    tab = synth.normal_bits(seed + 1, B * 2 * D, 0, 0.2, dtype)
+    tab = synth.normal_bits(seed + 1, B * 2 * D, 0, 0.2, dtype) if tab_bits is None else tab_bits
     t = dev_tensor(tab, dtype).view(B, 2, D)
     qs = torch.tensor([qscale], dtype=torch.float32, device="cuda")
     variant = ad.ln_modulate_fp8_variant(x, t[:, 1:2], t[:, 0:1], 1e-6, qs)
@@ -87,3 +88,30 @@ def test_non_finite_rows(ad):
 
 def test_flux_like_shape_sampled_rows(ad):
     case(ad, 1, 4608, 3072, 0.03, seed=11, rows=range(0, 4608, 5), expect="rows")
+
+
+@pytest.mark.parametrize("D", [3072, 2240])
+@pytest.mark.parametrize("qscale", [1e-30, 1e30])
+def test_scales_outside_the_division_window(ad, qscale, D):
+    # most quotients leave the range where the reciprocal correction is exact
+    # (huge ones saturate, tiny ones round to zero): whole rows take the
+    # checked quotient, on full and ragged widths
+    case(ad, 2, 40, D, qscale, seed=int(D + (qscale > 1)), expect="rows")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_exact_zero_outputs(ad, dtype):
+    # constant rows normalise to 0, so their outputs are 0 * op + shift: the
+    # +0 shift columns and the -0 ones with op = -1 give signed-zero outputs
+    # (outside the division window) beside ordinary values; random rows in
+    # between take the unchecked quotient in the same warps
+    B, N, D = 1, 16, 3072
+    xb = synth.normal_bits(21, B * N * D, 0.2, 1, dtype).reshape(N, D)
+    one = 0x3F80 if dtype == "bf16" else 0x3C00
+    xb[0::3] = one
+    tab = synth.normal_bits(22, B * 2 * D, 0, 0.2, dtype)
+    tab[0:D:5] = 0x0000
+    tab[3:D:7] = 0x8000
+    tab[D + 3:2 * D:7] = 0xC000   # scale -2: op = -1, so 0 * op = -0 and -0 + -0 = -0
+    ref = case(ad, B, N, D, 0.05, dtype, seed=21, x_bits=xb.reshape(-1), tab_bits=tab, expect="rows")
+    assert (ref[0] == 0x00).any() and (ref[0] == 0x80).any()
