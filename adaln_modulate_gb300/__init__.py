@@ -140,6 +140,27 @@ def _stream(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _guard(where: str, ref, inputs=(), outs=(), others=()) -> None:
+    """The C ABI takes raw pointers and cannot see where they point, so the
+    torch layer checks what it can: every tensor is a CUDA tensor on the
+    current device (``others``: no dtype rule), every entry of ``inputs``
+    has ``ref``'s dtype, and every output given as (tensor, element count,
+    dtypes) is contiguous with that many elements of one of those dtypes
+    (a smaller buffer would be written past its end)."""
+    tensors = [t for t in (ref, *inputs, *others, *(o[0] for o in outs)) if t is not None]
+    if not all(t.is_cuda for t in tensors):
+        raise ValueError(f"{where}: every tensor must be a CUDA tensor")
+    dev = _torch().cuda.current_device()
+    if any(t.get_device() != dev for t in tensors):
+        raise ValueError(f"{where}: every tensor must be on the current CUDA device (cuda:{dev})")
+    for t in inputs:
+        if t is not None and t.dtype != ref.dtype:
+            raise TypeError(f"{where}: a {t.dtype} operand with a {ref.dtype} input")
+    for t, numel, dtypes in outs:
+        if t is not None and (t.dtype not in dtypes or t.numel() != numel or not t.is_contiguous()):
+            raise ValueError(f"{where}: the output must be a contiguous tensor of {numel} elements of {dtypes}")
+
+
 def _rows_view(t, D: int, name: str):
     """(pointer, batch stride) of a (B, D) / (B, 1, D) row tensor."""
     if t.dim() == 3:
@@ -159,6 +180,7 @@ def ln_modulate(x, scale, shift, eps: float, out=None, flags: int = 0, stream=No
     contiguous (B, N, D) output."""
     torch = _torch()
     B, N, D = x.shape
+    _guard("ln_modulate", x, (scale, shift), ((out, B * N * D, (x.dtype,)),))
     if out is None:
         out = torch.empty((B, N, D), dtype=x.dtype, device=x.device)
     sp, ssb = _rows_view(scale, D, "scale")
@@ -195,6 +217,8 @@ def ln_modulate_fp8(x, scale, shift, eps: float, qscale, out=None, flags: int = 
     tensor (or writes ``out``, uint8 or float8_e4m3fn)."""
     torch = _torch()
     B, N, D, ((sp, ssb), (hp, hsb)) = _fp8_args(x, scale, shift, qscale)
+    _guard("ln_modulate_fp8", x, (scale, shift), ((out, B * N * D, (torch.uint8, torch.float8_e4m3fn)),),
+           others=(qscale,))
     if out is None:
         out = torch.empty((B, N, D), dtype=torch.float8_e4m3fn, device=x.device)
     st = capi.adaln_ln_modulate_fp8(out.data_ptr(), qscale.data_ptr(), x.data_ptr(), B, N, D, *x.stride(), sp, ssb,
@@ -244,12 +268,14 @@ def qk_head_layernorm(q, k, wq, bq, wk, bk, eps: float, q_out=None, k_out=None, 
     for t in (q, k):
         if t is not None and not t.is_contiguous():
             raise ValueError("q / k must be contiguous")
+    ref = q if q is not None else k
+    _guard("qk_head_layernorm", ref, (q, k, wq, bq, wk, bk),
+           ((q_out, rq * Dh, (ref.dtype,)), (k_out, rk * Dh, (ref.dtype,))))
     if q is not None and q_out is None:
         q_out = torch.empty_like(q)
     if k is not None and k_out is None:
         k_out = torch.empty_like(k)
     ptr = lambda t: t.data_ptr() if t is not None else None
-    ref = q if q is not None else k
     st = capi.adaln_qk_head_layernorm(ptr(q_out), ptr(q), rq, ptr(k_out), ptr(k), rk, Dh, ptr(wq),
                                       ptr(bq), ptr(wk), ptr(bk), float(eps), _dtype_code(ref), flags,
                                       _stream(stream))
@@ -263,6 +289,7 @@ def residual_gate_add(x, gate, y, out=None, flags: int = 0, stream=None):
     B, N, D = x.shape
     if not (x.is_contiguous() and y.is_contiguous()) or y.shape != x.shape:
         raise ValueError("x and y must be contiguous (B, N, D)")
+    _guard("residual_gate_add", x, (gate, y), ((out, B * N * D, (x.dtype,)),))
     if out is None:
         out = torch.empty_like(x)
     gp, gsb = _rows_view(gate, D, "gate")
@@ -283,6 +310,8 @@ def residual_gate_ln_modulate(x, gate, y, scale, shift, eps: float, r_out=None, 
     B, N, D = x.shape
     if not (x.is_contiguous() and y.is_contiguous()) or y.shape != x.shape:
         raise ValueError("x and y must be contiguous (B, N, D)")
+    _guard("residual_gate_ln_modulate", x, (gate, y, scale, shift),
+           ((r_out, B * N * D, (x.dtype,)), (out, B * N * D, (x.dtype,))))
     if r_out is None:
         r_out = torch.empty_like(x)
     if out is None:
@@ -324,6 +353,9 @@ def _operand(t, B: int, N: int, D: int, name: str, scalar_ok: bool = False):
 def _norm_call(fn, norm, x, scale, shift, eps, gate, y, r_out, out, flags, stream, variant=False):
     torch = _torch()
     B, N, D = x.shape
+    if not variant:
+        _guard("norm_scale_shift", x, (scale, shift, gate, y),
+               ((r_out if gate is not None else None, B * N * D, (x.dtype,)), (out, B * N * D, (x.dtype,))))
     sp, ssb, ssn, _ = _operand(scale, B, N, D, "scale")
     hp, hsb, hsn, _ = _operand(shift, B, N, D, "shift")
     if gate is not None:
@@ -373,6 +405,7 @@ def rmsnorm_scale_shift(x, scale, shift, eps: float, out=None, flags: int = 0, s
     with ``norm="rms"`` and no gate, through adaln_rmsnorm_scale_shift."""
     torch = _torch()
     B, N, D = x.shape
+    _guard("rmsnorm_scale_shift", x, (scale, shift), ((out, B * N * D, (x.dtype,)),))
     sp, ssb, ssn, _ = _operand(scale, B, N, D, "scale")
     hp, hsb, hsn, _ = _operand(shift, B, N, D, "shift")
     if out is None:
@@ -393,12 +426,13 @@ def qk_rmsnorm(q, k, wq, wk, eps: float, q_out=None, k_out=None, flags: int = 0,
     for t in (q, k):
         if t is not None and not t.is_contiguous():
             raise ValueError("q / k must be contiguous")
+    ref = q if q is not None else k
+    _guard("qk_rmsnorm", ref, (q, k, wq, wk), ((q_out, rq * Dh, (ref.dtype,)), (k_out, rk * Dh, (ref.dtype,))))
     if q is not None and q_out is None:
         q_out = torch.empty_like(q)
     if k is not None and k_out is None:
         k_out = torch.empty_like(k)
     ptr = lambda t: t.data_ptr() if t is not None else None
-    ref = q if q is not None else k
     st = capi.adaln_qk_rmsnorm(ptr(q_out), ptr(q), rq, ptr(k_out), ptr(k), rk, Dh, ptr(wq), ptr(wk), float(eps),
                                _dtype_code(ref), flags, _stream(stream))
     _check(st, "adaln_qk_rmsnorm")
@@ -423,6 +457,7 @@ def temb_table_slices(table, temb, out=None, flags: int = 0, stream=None):
     table = table.reshape(-1, table.shape[-1])
     if tuple(table.shape) != (K, D) or not table.is_contiguous() or not temb.is_contiguous():
         raise ValueError("table (K, D) and temb (B, S, K, D) must be contiguous")
+    _guard("temb_table_slices", temb, others=(table, out))
     if out is None:
         out = torch.empty((K, B, S, D), dtype=torch.float32, device=temb.device)
     if tuple(out.shape) != (K, B, S, D) or out.dtype != torch.float32 or not out.is_contiguous():
@@ -439,6 +474,7 @@ def bias_gelu_tanh(x, bias, out=None, flags: int = 0, stream=None):
     width = x.shape[-1]
     if not x.is_contiguous() or bias.numel() != width or not bias.is_contiguous():
         raise ValueError("x contiguous (..., width), bias (width,)")
+    _guard("bias_gelu_tanh", x, (bias,), ((out, x.numel(), (x.dtype,)),))
     if out is None:
         out = torch.empty_like(x)
     st = capi.adaln_bias_gelu_tanh(out.data_ptr(), x.data_ptr(), bias.data_ptr(),
