@@ -12,13 +12,20 @@
 // every bank (two wavefronts for 256 bytes).  Chunks past D/4 and tokens
 // past N are outside the tensor and arrive as zeros.
 //
-// Thread (l, h), l = tid / 4 the logical lane and h = tid % 4, owns tokens
-// 4h .. 4h+3 of lane l and reads 8 bytes of each of its four d-rows per
-// step.  Per tile: pass 1 (serial Welford of lane l for 4 tokens, two f32x2
-// chains) -> lane states in shared memory -> warp w folds token w and writes
-// mean / rstd -> pass 2 normalises, modulates with op = round(1 + scale) and
-// shift from a per-sample shared table, and stores 8 bytes per token.  The
-// next tile's boxes are prefetched into L2 while the current one runs.
+// Thread (l, h), l = tid / 2 the logical lane and h = tid % 2, owns tokens
+// 8h .. 8h+7 of lane l and reads 16 bytes of each of its four d-rows per
+// step (a warp reads 512 contiguous bytes).  Per tile: pass 1 (serial
+// Welford of lane l for 8 tokens, four f32x2 chains) -> lane states in
+// shared memory -> warp w folds tokens 2w and 2w+1 and writes mean / rstd ->
+// pass 2 normalises, modulates with op = round(1 + scale) and shift from a
+// per-sample shared table, and stores 8 bytes per token.
+//
+// 256 threads of at most 128 registers and about 111 KB of shared memory for
+// D <= 2560, so two CTAs fit on an SM: with programmatic dependent launch the
+// next call's CTAs become resident while this call's still run, and each
+// asks L2 for its first tile before it waits for this grid to finish, so its
+// tile is mostly in L2 by the time it may load it.  The next tile of a CTA
+// that loops over several is prefetched into L2 while the current one runs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -31,7 +38,7 @@
 namespace adaln {
 
 constexpr int kTT = 16;             // tokens per tile
-constexpr int kTTThreads = 512;     // (128 lanes) x (4 token groups)
+constexpr int kTTThreads = 256;     // (128 lanes) x (2 token groups of 8)
 constexpr int kTTRowBytes = kTT * 2;
 constexpr int kStepBytes = 512 * kTTRowBytes;   // one box: 128 chunks x 4 elements x 16 tokens
 constexpr int kPlaneBytes = 128 * kTTRowBytes;  // one e-plane of a box
@@ -39,7 +46,8 @@ constexpr int kTTPitch = 154;       // lane-state row pitch: 4 * pitch = 8 (mod 
 constexpr int kWaitSpins = 1 << 22; // bounded mbarrier waits
 constexpr int kTTMaxNI = 10;        // D <= 5120
 constexpr int kFillPer = (kTTMaxNI * 512 / 2 + kTTThreads - 1) / kTTThreads;  // table pairs per thread
-static_assert(kTTThreads / 32 == kTT, "one fold warp per token");
+constexpr int kTTWarps = kTTThreads / 32;
+static_assert(2 * kTTWarps == kTT, "two fold tokens per warp");
 
 // Timed-out mbarrier waits of the TMA tile kernel on this device (should stay 0).
 __device__ unsigned int g_tma_wait_timeouts;
@@ -77,7 +85,7 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, 
 }
 
 template <DT T, int NI>
-__global__ void __launch_bounds__(kTTThreads, 1)
+__global__ void __launch_bounds__(kTTThreads, 2)
 ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int64_t N, int D,
                      const uint16_t *scale, int64_t s_scale_b, const uint16_t *shift, int64_t s_shift_b,
                      float eps, int64_t tiles_per_b, int64_t ntiles) {
@@ -90,15 +98,15 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int l = tid >> 2;
-    const int h = tid & 3;
+    const int l = tid >> 1;
+    const int h = tid & 1;
     const int nvec = D >> 2;
     const float Df = (float)D;
     const uint32_t dyn_s = (uint32_t)__cvta_generic_to_shared(tt_dyn);
     const uint32_t tile_s = (dyn_s + 1023u) & ~1023u;  // [step][e][chunk][16 tokens]
     uint32_t *opsh = reinterpret_cast<uint32_t *>(tt_dyn + (tile_s - dyn_s) + NI * kStepBytes);
     const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(&bar[0]);
-    const uint32_t my_s = tile_s + (uint32_t)(kTTRowBytes * l + 8 * h);  // (step 0, e 0) of this thread
+    const uint32_t my_s = tile_s + (uint32_t)(kTTRowBytes * l + 16 * h);  // (step 0, e 0) of this thread
 
     // Launch parameters are not data of the previous kernel: read them, fetch
     // the tensor map's descriptor and set up the barriers before waiting on
@@ -112,8 +120,18 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
         for (int i = 0; i < NI; ++i) mbar_init(bar_s + 8 * i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\nfence.proxy.async.shared::cta;" ::: "memory");
         const int64_t b0 = (int64_t)blockIdx.x / tiles_per_b;
+        const int64_t f0 = ((int64_t)blockIdx.x - b0 * tiles_per_b) * kTT;
         first_tile[0] = b0;
-        first_tile[1] = ((int64_t)blockIdx.x - b0 * tiles_per_b) * kTT;
+        first_tile[1] = f0;
+        // Ask L2 for the first tile and its sample's scale / shift rows now,
+        // while the previous kernel may still be running.  A prefetch is only
+        // a hint with no effect on what later loads return: L2 is where every
+        // SM's accesses to global memory meet, so the loads issued after the
+        // wait still see everything the previous kernel wrote.
+#pragma unroll
+        for (int i = 0; i < NI; ++i) tma_prefetch_4d(&tmx, (int)f0, 128 * i, 0, (int)b0);
+        prefetch_l2(scale + b0 * s_scale_b, (uint64_t)D * 2);
+        prefetch_l2(shift + b0 * s_shift_b, (uint64_t)D * 2);
     }
     __syncthreads();
     pdl_wait();
@@ -159,7 +177,7 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
                 }
             }
         }
-        if (t == blockIdx.x && warp == kTT - 1) {
+        if (t == blockIdx.x && warp == kTTWarps - 1) {
             // fold plan of lane group u (read by every fold warp), while the boxes land
             const int u = tid & 31;
             const FoldPlan pl = (D % 512 == 0) ? fold_plan_uniform(NI) : fold_plan_runtime(u, nvec);
@@ -168,31 +186,34 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
             for (int k = 0; k < 16; ++k) plan_s[k][u] = f[k];
         }
 
-        // pass 1: Welford of lane l for tokens (4h, 4h+1) and (4h+2, 4h+3)
+        // pass 1: Welford of lane l for the token pairs (8h + 2k, 8h + 2k + 1)
         bool ok = true;
-        f2_t ma = f2(0.f, 0.f), qa = ma, mb = ma, qb = ma;
+        f2_t m[4], q[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m[k] = q[k] = f2(0.f, 0.f);
         static_for<0, NI>([&](auto I) {
             constexpr int i = decltype(I)::value;
             ok = mbar_wait(bar_s + 8 * i, parity) && ok;
             if (128 * i + l < nvec) {
                 static_for<0, 4>([&](auto E) {
                     constexpr int e = decltype(E)::value;
-                    uint32_t v[2];
-                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
-                                 : "=r"(v[0]), "=r"(v[1])
+                    uint32_t v[4];
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
                                  : "r"(my_s + (uint32_t)(i * kStepBytes + e * kPlaneBytes)));
                     constexpr float r = Rcp<4 * i + e + 1>::value;
-                    push2(ma, qa, f2(lo_f32<T>(v[0]), hi_f32<T>(v[0])), r);
-                    push2(mb, qb, f2(lo_f32<T>(v[1]), hi_f32<T>(v[1])), r);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) push2(m[k], q[k], f2(lo_f32<T>(v[k]), hi_f32<T>(v[k])), r);
                 });
             }
         });
         {
             const int si = l + 8 * (l >> 5);
-            f2_split(ma, st_mean[4 * h][si], st_mean[4 * h + 1][si]);
-            f2_split(mb, st_mean[4 * h + 2][si], st_mean[4 * h + 3][si]);
-            f2_split(qa, st_m2[4 * h][si], st_m2[4 * h + 1][si]);
-            f2_split(qb, st_m2[4 * h + 2][si], st_m2[4 * h + 3][si]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                f2_split(m[k], st_mean[8 * h + 2 * k][si], st_mean[8 * h + 2 * k + 1][si]);
+                f2_split(q[k], st_m2[8 * h + 2 * k][si], st_m2[8 * h + 2 * k + 1][si]);
+            }
         }
         if (new_table) {
 #pragma unroll
@@ -214,52 +235,60 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
             return;
         }
 
-        // warp w folds token w (a token past N folds zeros and is not stored)
+        // warp w folds tokens 2w and 2w + 1 (a token past N folds zeros and is
+        // not stored)
         {
             const int u = tid & 31;
             const int i0 = (u & 7) + 32 * (u >> 3) + 8 * (u >> 3);
-            const float *mw = st_mean[warp], *qw = st_m2[warp];
             FoldPlan plan;
             float *f = reinterpret_cast<float *>(&plan);
 #pragma unroll
             for (int k = 0; k < 16; ++k) f[k] = plan_s[k][u];
-            float mean, m2;
-            fold128_s8(f2(mw[i0], mw[i0 + 8]), f2(qw[i0], qw[i0 + 8]), f2(mw[i0 + 16], mw[i0 + 24]),
-                       f2(qw[i0 + 16], qw[i0 + 24]), plan, mean, m2);
-            const float rstd = finish_rstd(m2, Df, eps);
-            if (u == 0) {
-                fin[0][warp] = mean;
-                fin[1][warp] = rstd;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int tk = 2 * warp + k;
+                const float *mw = st_mean[tk], *qw = st_m2[tk];
+                float mean, m2;
+                fold128_s8(f2(mw[i0], mw[i0 + 8]), f2(qw[i0], qw[i0 + 8]), f2(mw[i0 + 16], mw[i0 + 24]),
+                           f2(qw[i0 + 16], qw[i0 + 24]), plan, mean, m2);
+                const float rstd = finish_rstd(m2, Df, eps);
+                if (u == 0) {
+                    fin[0][tk] = mean;
+                    fin[1][tk] = rstd;
+                }
             }
         }
         __syncthreads();
 
-        // pass 2: tokens 4h .. 4h+3 of lane l
-        const f2_t meanA = f2(fin[0][4 * h], fin[0][4 * h + 1]);
-        const f2_t meanB = f2(fin[0][4 * h + 2], fin[0][4 * h + 3]);
-        const f2_t rstdA = f2(fin[1][4 * h], fin[1][4 * h + 1]);
-        const f2_t rstdB = f2(fin[1][4 * h + 2], fin[1][4 * h + 3]);
-        const int nmine = (int)imin64(4, N - n0 - 4 * h);  // tokens of this group inside N
-        uint16_t *ob = out + (b * N + n0 + 4 * h) * (int64_t)D + 4 * l;
+        // pass 2: tokens 8h .. 8h+7 of lane l
+        f2_t mean2[4], rstd2[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            mean2[k] = f2(fin[0][8 * h + 2 * k], fin[0][8 * h + 2 * k + 1]);
+            rstd2[k] = f2(fin[1][8 * h + 2 * k], fin[1][8 * h + 2 * k + 1]);
+        }
+        const int nmine = (int)imin64(8, N - n0 - 8 * h);  // tokens of this group inside N
+        uint16_t *ob = out + (b * N + n0 + 8 * h) * (int64_t)D + 4 * l;
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
             if (128 * i + l < nvec) {
                 const uint4 os = *reinterpret_cast<const uint4 *>(opsh + 4 * (128 * i + l));
-                float y[4][4];  // [element e of the chunk][token]
+                float y[4][8];  // [element e of the chunk][token]
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    uint32_t v[2];
-                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
-                                 : "=r"(v[0]), "=r"(v[1])
+                    uint32_t v[4];
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
                                  : "r"(my_s + (uint32_t)(i * kStepBytes + e * kPlaneBytes)));
-                    float x0, x1, x2, x3;
-                    unpack_again<T>(v[0], x0, x1);
-                    unpack_again<T>(v[1], x2, x3);
-                    f2_split(f2_mul(f2_sub(f2(x0, x1), meanA), rstdA), y[e][0], y[e][1]);
-                    f2_split(f2_mul(f2_sub(f2(x2, x3), meanB), rstdB), y[e][2], y[e][3]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float xa, xb;
+                        unpack_again<T>(v[k], xa, xb);
+                        f2_split(f2_mul(f2_sub(f2(xa, xb), mean2[k]), rstd2[k]), y[e][2 * k], y[e][2 * k + 1]);
+                    }
                 }
 #pragma unroll
-                for (int tk = 0; tk < 4; ++tk) {
+                for (int tk = 0; tk < 8; ++tk) {
                     if (tk < nmine) {
                         uint32_t o[2];
                         o[0] = add16x2<T>(mul16x2<T>(pack_rn<T>(y[0][tk], y[1][tk]), os.x), os.y);

@@ -13,7 +13,9 @@ Timing: W untimed warm-up steps, then exactly K steps timed as one region
 are larger than L2: the op's inputs and output are replicated into R sets
 that together cover at least 4x the L2, and step k uses set k mod R, so no
 step finds its inputs in L2.  The K steps are launched from CUDA graphs,
-each kernel with programmatic dependent launch.  As a diagnostic, the same
+each kernel with programmatic dependent launch; every graph is replayed once
+during warm-up, and a short spin kernel queued ahead of the start event keeps
+the host's graph submission out of the timed region.  As a diagnostic, the same
 op is also timed one call at a time with L2 flushed before each call (a
 256 MiB buffer written, then another read) and CUDA events around each.
 Clocks and throttle reasons are sampled with nvidia-smi during the timed
@@ -49,6 +51,7 @@ METRIC = "fused LN+modulate GB/s and µs/call at (2,1024,2240) bf16; % of HBM ro
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 256 << 20
 MAX_SETS = 64  # rotating input sets per workload
+SPIN_CYCLES = 200_000  # about 0.1 ms at 2 GHz: longer than the submission of the first graph
 
 
 # ------------------------------------------------------------ utilities
@@ -440,12 +443,20 @@ def time_block(calls, steps, warmup, on_begin=None, on_end=None):
             graphs[n] = g
     torch.cuda.synchronize()
     full, rest = divmod(steps, R)
-    for k in range(max(1, -(-warmup // R))):
+    # warm-up: W steps (at least one replay of every graph the timed region
+    # uses, so that no graph is uploaded or run for the first time inside it)
+    for g in graphs.values():
+        g.replay()
+    for k in range(max(0, -(-warmup // R) - 1)):
         graphs[R].replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if on_begin:
         on_begin()
+    # A short spin kernel ahead of the start event keeps the stream busy while
+    # the host submits the graphs, so the region times the K steps on the
+    # device and not the host's submission latency in front of the first one.
+    torch.cuda._sleep(SPIN_CYCLES)
     e0.record()
     for _ in range(full):
         graphs[R].replay()
