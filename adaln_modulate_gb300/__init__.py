@@ -59,6 +59,7 @@ _SIGS = {
     "adaln_bias_gelu_tanh": ([_P, _P, _P, _I, _I, _INT, _U, _P], _INT),
     "adaln_can_bias_gelu_tanh": ([_P, _P, _P, _I, _I, _INT, _U], _INT),
     "adaln_bias_gelu_tanh_noalloc": ([_P, _P, _P, _I, _I, _INT, _U, _P], _INT),
+    "adaln_copy_reference": ([_P, _P, _I, _U, _P], _INT),
     "adaln_tma_wait_timeouts": ([_P], _INT),
     "adaln_residual_gate_ln_modulate": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _I, _F, _INT, _U, _P],
                                         _INT),
@@ -481,6 +482,20 @@ def bias_gelu_tanh(x, bias, out=None, flags: int = 0, stream=None):
                                    x.numel() // width, width, _dtype_code(x), flags, _stream(stream))
     _check(st, "adaln_bias_gelu_tanh")
     return out
+
+
+def copy_reference(src, dst, nbytes: Optional[int] = None, flags: int = 0, stream=None):
+    """Same-byte device copy (the measurement yardstick): the first nbytes
+    (default: all) bytes of src into dst, both CUDA tensors on this device."""
+    _guard("copy_reference", dst, others=(src,))
+    if not src.is_contiguous() or not dst.is_contiguous():
+        raise ValueError("copy_reference: src and dst must be contiguous")
+    n = src.numel() * src.element_size() if nbytes is None else int(nbytes)
+    if n > src.numel() * src.element_size() or n > dst.numel() * dst.element_size():
+        raise ValueError("copy_reference: nbytes beyond a tensor")
+    st = capi.adaln_copy_reference(dst.data_ptr(), src.data_ptr(), n, flags, _stream(stream))
+    _check(st, "adaln_copy_reference")
+    return dst
 
 
 def init(device: Optional[int] = None) -> None:

@@ -16,7 +16,7 @@ using namespace adaln;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevices = kApiMaxDevices;
 
 struct DevState {
     DeviceInfo info;
@@ -316,6 +316,14 @@ adaln_status finish_launch(cudaError_t e) { return e == cudaSuccess ? ADALN_OK :
 }  // namespace
 
 namespace adaln {
+
+adaln_status api_current_device(int *dev) { return current_device(dev); }
+adaln_status api_device_info(int dev, DeviceInfo *out) { return device_info(dev, out); }
+adaln_status api_cuda_fail(cudaError_t e) { return cuda_fail(e); }
+adaln_status api_fail_msg(const char *msg) {
+    snprintf(g_err, sizeof(g_err), "%s", msg);
+    return ADALN_E_CUDA;
+}
 
 int blocks_per_sm_cached(const void *kernel, int threads, size_t smem) {
     struct Entry {

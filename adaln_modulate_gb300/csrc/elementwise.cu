@@ -47,6 +47,16 @@ template <DT T, int EPT>
 __global__ void __launch_bounds__(kEwThreads)
 gate_add_kernel(uint16_t *out, const uint16_t *x, const uint16_t *gate, int64_t s_gate_b,
                 const uint16_t *y, int64_t nvec, int64_t ND, int64_t D) {
+    // ask L2 for this CTA's first x and y elements before waiting on the
+    // previous kernel (a hint only: loads after the wait still see its writes)
+    if (threadIdx.x == 0) {
+        const int64_t e0 = (int64_t)blockIdx.x * kEwThreads * EPT;
+        const int64_t e1 = imin64(e0 + (int64_t)kEwThreads * EPT, nvec * EPT);
+        if (e1 > e0) {
+            prefetch_l2(x + e0, (uint64_t)(e1 - e0) * 2);
+            prefetch_l2(y + e0, (uint64_t)(e1 - e0) * 2);
+        }
+    }
     pdl_wait();
     pdl_trigger();
     constexpr int R = EPT / 2;

@@ -29,15 +29,17 @@ static __device__ __align__(256) uint16_t g_noalloc_scratch[2 * kTableEntries];
 
 namespace {
 
-constexpr int kMaxDev = 64;
-
 struct NoallocDev {
     uint16_t *tables = nullptr;  // device address of g_noalloc_scratch on this device
     bool built[2] = {false, false};
 };
 
 std::mutex g_mu;
-NoallocDev g_state[kMaxDev];
+NoallocDev g_state[kApiMaxDevices];
+
+// Both storage types' tables fit the array, whatever the call's rows and
+// width: the scratch holds lookup tables, not data of the call.
+static_assert(2 * kTableEntries * sizeof(uint16_t) <= kNoallocScratchBytes, "both tables fit");
 
 }  // namespace
 }  // namespace adaln
@@ -50,12 +52,9 @@ extern "C" adaln_status adaln_bias_gelu_tanh_noalloc(void *out, const void *x, c
     // the same argument rules as adaln_bias_gelu_tanh
     adaln_status st = adaln_can_bias_gelu_tanh(out, x, bias, rows, width, dtype, flags);
     if (st != ADALN_OK) return st;
-    // the call needs one table of its storage type inside the fixed scratch
-    const size_t need = (size_t)(dtype + 1) * kTableEntries * sizeof(uint16_t);
-    if (need > kNoallocScratchBytes) return ADALN_E_SHAPE;
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDev) return ADALN_E_CUDA;
+    DeviceInfo info;  // the per-device properties the other entry points use, cached
+    if ((st = api_current_device(&dev)) != ADALN_OK || (st = api_device_info(dev, &info)) != ADALN_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     uint16_t *tables = nullptr;
     {
@@ -64,27 +63,32 @@ extern "C" adaln_status adaln_bias_gelu_tanh_noalloc(void *out, const void *x, c
         // caller's stream and wait for it
         std::lock_guard<std::mutex> lk(g_mu);
         NoallocDev &d = g_state[dev];
-        if (!d.tables) {
-            void *p = nullptr;
-            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-            if (e != cudaSuccess) return ADALN_E_CUDA;
-            d.tables = (uint16_t *)p;
-        }
         if (!d.built[dtype]) {
+            // the build runs on the caller's stream and is waited for: inside a
+            // stream capture it would become part of the caller's graph and the
+            // wait would break the capture, so refuse (before any other CUDA
+            // call of the set-up) and leave the stream as it is
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            cudaError_t e = cudaStreamIsCapturing(s, &cs);
+            if (e != cudaSuccess) return api_cuda_fail(e);
+            if (cs != cudaStreamCaptureStatusNone)
+                return api_fail_msg(
+                    "GELU table of this storage type not set up on this device: make the first "
+                    "adaln_bias_gelu_tanh_noalloc call before capturing the stream");
+            if (!d.tables) {
+                void *p = nullptr;
+                e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+                if (e != cudaSuccess) return api_cuda_fail(e);
+                d.tables = (uint16_t *)p;
+            }
             e = launch_gelu_table_init(d.tables + (size_t)dtype * kTableEntries, dtype, s);
             if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-            if (e != cudaSuccess) return ADALN_E_CUDA;
+            if (e != cudaSuccess) return api_cuda_fail(e);
             d.built[dtype] = true;
         }
         tables = d.tables;
     }
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return ADALN_E_CUDA;
-    DeviceInfo info;
-    info.device = dev;
-    info.sms = sms;
     GeluArgs a{out, x, bias, rows, width, tables + (size_t)dtype * kTableEntries};
-    e = launch_bias_gelu_tanh(a, dtype, (flags & ADALN_FLAG_PDL) != 0, s, info);
-    return e == cudaSuccess ? ADALN_OK : ADALN_E_CUDA;
+    const cudaError_t e = launch_bias_gelu_tanh(a, dtype, (flags & ADALN_FLAG_PDL) != 0, s, info);
+    return e == cudaSuccess ? ADALN_OK : api_cuda_fail(e);
 }

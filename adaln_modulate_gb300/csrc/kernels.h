@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/adaln.h"
+
 namespace adaln {
 
 struct DeviceInfo {
@@ -114,6 +116,17 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// Host helpers of the C ABI (api.cu) for entry points defined in other
+// files: the current device (an ordinal past the library's 64 per-device
+// slots is an error with its own text), its cached properties, and the text
+// that adaln_last_cuda_error() returns after a failure (a CUDA error, or a
+// message of the caller's).  Each returns ADALN_OK or ADALN_E_CUDA.
+adaln_status api_current_device(int *dev);
+adaln_status api_device_info(int dev, DeviceInfo *out);
+adaln_status api_cuda_fail(cudaError_t e);
+adaln_status api_fail_msg(const char *msg);
+constexpr int kApiMaxDevices = 64;
 
 // Resident blocks per SM of a kernel at a block size / dynamic smem, cached
 // per (kernel, block size, smem); every device this library drives is the

@@ -215,6 +215,16 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
                   const uint16_t *wk, const uint16_t *bk, float eps) {
     __shared__ __align__(16) float aff[2][2][128];  // [q / k][w / b][column]
     constexpr int NL = 32;
+    // ask L2 for the warp's first 16 rows before waiting on the previous
+    // kernel (a hint only: loads after the wait still see its writes)
+    if ((threadIdx.x & 31) == 0) {
+        const int64_t total = rows_q + rows_k;
+        const int64_t nb = (((int64_t)blockIdx.x * kQkThreads + threadIdx.x) >> 5) * 16;
+        const int64_t ne = imin64(nb + 16, total);
+        if (nb < rows_q) prefetch_l2(q + nb * 128, (uint64_t)(imin64(ne, rows_q) - nb) * 256);
+        const int64_t ks = nb > rows_q ? nb : rows_q;
+        if (ne > ks) prefetch_l2(k + (ks - rows_q) * 128, (uint64_t)(ne - ks) * 256);
+    }
     pdl_wait();
     pdl_trigger();
     for (int c = threadIdx.x; c < 128; c += kQkThreads) {

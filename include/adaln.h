@@ -476,6 +476,21 @@ adaln_status adaln_can_bias_gelu_tanh(const void *out, const void *x, const void
                                       int dtype, uint32_t flags);
 
 /* ------------------------------------------------------------------------
+ * adaln_copy_reference
+ *   Copies `bytes` bytes from src to dst on `stream` with a kernel built like
+ *   the ops' streaming kernels (32-byte accesses that bypass L1, a persistent
+ *   grid sized from the SM count, ADALN_FLAG_PDL as for the ops).  The pages
+ *   have no counterpart: it is the same-byte yardstick that measurements put
+ *   beside each op (an op that moves R + W bytes is compared with a copy of
+ *   (R + W) / 2 bytes).
+ *   dst, src: device pointers, 32-byte aligned (else ADALN_E_ALIGN), not
+ *   overlapping (else ADALN_E_OVERLAP); bytes in [1, 2^46] (else
+ *   ADALN_E_SHAPE); flags 0 or ADALN_FLAG_PDL (else ADALN_E_VALUE).
+ *   Asynchronous; returns ADALN_E_CUDA if the launch fails.
+ * ---------------------------------------------------------------------- */
+adaln_status adaln_copy_reference(void *dst, const void *src, int64_t bytes, uint32_t flags, void *stream);
+
+/* ------------------------------------------------------------------------
  * adaln_bias_gelu_tanh_noalloc
  *   The same operation, arguments, limits and results (bit for bit) as
  *   adaln_bias_gelu_tanh, for callers that cannot let a library allocate
@@ -492,14 +507,18 @@ adaln_status adaln_can_bias_gelu_tanh(const void *out, const void *x, const void
  *   allocating routine.  The caller still allocates and owns x, bias, out.
  *
  *   Memory held: 256 KiB (one 65536-entry table per storage type) on every
- *   GPU that loads the library, until the process exits.  Every call needs
- *   one 128 KiB table inside it; a call whose table would not fit returns
- *   ADALN_E_SHAPE (no bf16 / fp16 call does).
+ *   GPU that loads the library, until the process exits.  The array holds
+ *   lookup tables, not data of the call: its size does not depend on rows
+ *   or width, both storage types' tables always fit, and the limits on
+ *   rows and width are those of adaln_bias_gelu_tanh.
  *
  *   Set-up: the first call on a device for a storage type (made with that
  *   device current) looks up the array's device address and fills that
- *   storage type's table on `stream`, then waits for the stream to finish.
- *   Make that first call before capturing `stream` into a CUDA graph.  The
+ *   storage type's table on `stream`, then waits for the stream to finish
+ *   (so it runs after work already queued on `stream`).  Make that first
+ *   call before capturing `stream` into a CUDA graph: a first call on a
+ *   stream that is being captured returns ADALN_E_CUDA, with a message from
+ *   adaln_last_cuda_error(), and leaves the capture untouched.  The
  *   table is written only by that first call; later calls only read the
  *   shared array, and nothing in it has to start at zero.  A later call
  *   that overlaps that first call's table build on another stream would

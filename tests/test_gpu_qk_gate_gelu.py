@@ -104,10 +104,11 @@ def test_gelu_wan_full(ad, dtype):
     bias = w.tensors["bias"].draw(dtype)
     out = ad.bias_gelu_tanh(dev_tensor(x, dtype), dev_tensor(bias, dtype))
     got = host_bits(out)
-    # every row of a strided sample, and the whole first and last 64 rows
-    rows_s = sorted(set(range(0, rows, 97)) | set(range(64)) | set(range(rows - 64, rows)))
-    ids, ref = oracle.bias_gelu_tanh(x, bias, rows, width, dtype, rows=rows_s, threads=THREADS)
-    assert_bits_equal(got[ids], ref, dtype, f"wan {dtype}")
+    del out
+    # the whole output, all 32760 x 13824 elements, against the oracle
+    ids, ref = oracle.bias_gelu_tanh(x, bias, rows, width, dtype, threads=THREADS)
+    assert ids.size == rows
+    assert_bits_equal(got, ref, dtype, f"wan {dtype}")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])

@@ -1,10 +1,16 @@
 """Pins of the oracle's storage conversions against library routines.
 
 bf16 <- f32 against torch's round-to-nearest-even conversion, fp16 <- f32
-against numpy's, and both decodings exhaustively.  The f32 inputs are every
-value of the upper 16 bits combined with low halves chosen to hit every
-rounding case (exact, below / at / above the halfway point, odd and even).
+against numpy's (and, on every one of the 2^32 binary32 bit patterns, both
+against torch's round-to-nearest-even conversions), and both
+decodings exhaustively.  A stratified sample (every value of the upper 16
+bits combined with low halves chosen to hit every rounding case: exact,
+below / at / above the halfway point, odd and even) runs first as a quick
+check.
 """
+import concurrent.futures
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -64,3 +70,46 @@ def test_roundtrip_is_identity(oracle_lib, dtype):
     back = oracle.to16(f, dtype)
     keep = ~np.isnan(f)
     assert np.array_equal(back[keep], h[keep])
+
+
+CHUNK = 1 << 24
+
+
+def _exhaustive_chunk(c):
+    """Conversions of the binary32 patterns [c * CHUNK, (c + 1) * CHUNK) by the
+    oracle and by the library routines: returns (mismatches, examples)."""
+    u = np.arange(c * CHUNK, (c + 1) * CHUNK, dtype=np.uint64).astype(np.uint32)
+    f = u.view(np.float32)
+    nan = np.isnan(f)
+    bad, ex = 0, []
+    got = oracle.to16(f, "bf16")
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    miss = (got != ref) & ~nan
+    miss |= nan & (got != 0x7FC0)
+    if miss.any():
+        i = np.flatnonzero(miss)
+        bad += i.size
+        ex += [("bf16", hex(int(u[j])), hex(int(got[j])), hex(int(ref[j]))) for j in i[:3]]
+    got = oracle.to16(f, "fp16")
+    ref = torch.from_numpy(f).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    miss = (got != ref) & ~nan
+    miss |= nan & (got != 0x7E00)
+    if miss.any():
+        i = np.flatnonzero(miss)
+        bad += i.size
+        ex += [("fp16", hex(int(u[j])), hex(int(got[j])), hex(int(ref[j]))) for j in i[:3]]
+    return bad, ex
+
+
+def test_encode_every_binary32_pattern(oracle_lib):
+    """All 2^32 binary32 inputs: the oracle's bf16 and fp16 equal torch's
+    (every non-NaN input), and every NaN input gives the canonical quiet
+    NaN."""
+    n = (1 << 32) // CHUNK
+    workers = max(1, min(8, os.cpu_count() or 1))
+    bad, ex = 0, []
+    with concurrent.futures.ThreadPoolExecutor(workers) as pool:
+        for b, e in pool.map(_exhaustive_chunk, range(n)):
+            bad += b
+            ex += e
+    assert bad == 0, (bad, ex[:8])
