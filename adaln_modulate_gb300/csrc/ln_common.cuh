@@ -167,6 +167,35 @@ __device__ __forceinline__ void fold128_s8(f2_t m01, f2_t q01, f2_t m23, f2_t q2
     m2 = q0;
 }
 
+// The same fold for two tokens at once: each f32x2 holds one lane's state of
+// tokens A (x) and B (y), so every step is the per-token step of fold128_s8
+// on both tokens in one instruction (the same IEEE operations in the same
+// order for each token, hence the same bits).  s0..s3 are the thread's lanes
+// l0, l0 + 8, l0 + 16, l0 + 24.
+__device__ __forceinline__ void shfl_stage_p2(f2_t &m, f2_t &q, int mask, float coef, float na) {
+    const f2_t pm = __shfl_xor_sync(0xffffffffu, m, mask);
+    const f2_t pq = __shfl_xor_sync(0xffffffffu, q, mask);
+    const bool lower = (threadIdx.x & mask) == 0;
+    const f2_t lo = lower ? m : pm, up = lower ? pm : m;
+    const f2_t delta = f2_sub(up, lo);
+    m = f2_fma(delta, f2(coef, coef), lo);
+    q = f2_fma(f2_mul(f2_mul(delta, delta), f2(na, na)), f2(coef, coef), f2_add(q, pq));
+}
+
+__device__ __forceinline__ void fold128_s8_x2(f2_t m0, f2_t q0, f2_t m1, f2_t q1, f2_t m2, f2_t q2, f2_t m3,
+                                              f2_t q3, const FoldPlan &p, f2_t &mean, f2_t &m2out) {
+    chan_p2(m0, q0, m2, q2, f2(p.c16[0], p.c16[0]), f2(p.n16[0], p.n16[0]));  // offset 16: (s0, s2)
+    chan_p2(m1, q1, m3, q3, f2(p.c16[1], p.c16[1]), f2(p.n16[1], p.n16[1]));  //            (s1, s3)
+    chan_p2(m0, q0, m1, q1, f2(p.c8, p.c8), f2(p.n8, p.n8));                  // offset 8
+    shfl_stage_p2(m0, q0, 4, p.c[0], p.n[0]);
+    shfl_stage_p2(m0, q0, 2, p.c[1], p.n[1]);
+    shfl_stage_p2(m0, q0, 1, p.c[2], p.n[2]);
+    shfl_stage_p2(m0, q0, 16, p.c[3], p.n[3]);
+    shfl_stage_p2(m0, q0, 8, p.c[4], p.n[4]);
+    mean = m0;
+    m2out = q0;
+}
+
 // RMSNorm: the 128 lanes' sums of squares folded in the butterfly order of
 // fold128_s8 (offsets 16 and 8 inside the thread, then 4, 2, 1, 64, 32
 // across threads) with plain additions.  IEEE addition commutes, so both

@@ -235,8 +235,8 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
             return;
         }
 
-        // warp w folds tokens 2w and 2w + 1 (a token past N folds zeros and is
-        // not stored)
+        // warp w folds tokens 2w and 2w + 1 together, one f32x2 lane per token
+        // (a token past N folds zeros and is not stored)
         {
             const int u = tid & 31;
             const int i0 = (u & 7) + 32 * (u >> 3) + 8 * (u >> 3);
@@ -244,18 +244,21 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
             float *f = reinterpret_cast<float *>(&plan);
 #pragma unroll
             for (int k = 0; k < 16; ++k) f[k] = plan_s[k][u];
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int tk = 2 * warp + k;
-                const float *mw = st_mean[tk], *qw = st_m2[tk];
-                float mean, m2;
-                fold128_s8(f2(mw[i0], mw[i0 + 8]), f2(qw[i0], qw[i0 + 8]), f2(mw[i0 + 16], mw[i0 + 24]),
-                           f2(qw[i0 + 16], qw[i0 + 24]), plan, mean, m2);
-                const float rstd = finish_rstd(m2, Df, eps);
-                if (u == 0) {
-                    fin[0][tk] = mean;
-                    fin[1][tk] = rstd;
-                }
+            const float *mA = st_mean[2 * warp], *qA = st_m2[2 * warp];
+            const float *mB = st_mean[2 * warp + 1], *qB = st_m2[2 * warp + 1];
+            f2_t mean2, m22;
+            fold128_s8_x2(f2(mA[i0], mB[i0]), f2(qA[i0], qB[i0]), f2(mA[i0 + 8], mB[i0 + 8]),
+                          f2(qA[i0 + 8], qB[i0 + 8]), f2(mA[i0 + 16], mB[i0 + 16]), f2(qA[i0 + 16], qB[i0 + 16]),
+                          f2(mA[i0 + 24], mB[i0 + 24]), f2(qA[i0 + 24], qB[i0 + 24]), plan, mean2, m22);
+            float meanA, meanB, m2A, m2B;
+            f2_split(mean2, meanA, meanB);
+            f2_split(m22, m2A, m2B);
+            const float rstdA = finish_rstd(m2A, Df, eps), rstdB = finish_rstd(m2B, Df, eps);
+            if (u == 0) {
+                fin[0][2 * warp] = meanA;
+                fin[1][2 * warp] = rstdA;
+                fin[0][2 * warp + 1] = meanB;
+                fin[1][2 * warp + 1] = rstdB;
             }
         }
         __syncthreads();
