@@ -316,6 +316,12 @@ def make_workloads(dev, which, n_sets=None, flags=0):
             base.append(torch.empty_like(base[0]))
             out[key] = ([(lambda x=x, b=b, o=o: ad.bias_gelu_tanh(x, b, out=o, flags=flags))
                          for x, b, o in copies(base, sets_for(nb))], nb, w.name)
+    if "copy_sana" in which:
+        # the same-byte yardstick of the headline as a workload of its own
+        # (profiling runs): the library copy kernel moving the Sana bytes
+        nb = ln_bytes(2, 1024, 2240)
+        out["copy_sana"] = (copy_calls(dev, nb, flags=flags), nb,
+                            "adaln_copy_reference, the Sana LN+modulate's byte count (9,184,000 B copied)")
     return out
 
 
@@ -824,7 +830,8 @@ def main():
     p.add_argument("--quick", action="store_true", help="headline only (for profiler runs)")
     p.add_argument("--only", default="sana",
                    choices=["sana", "sana_nmod2", "tiny", "glm_ln", "glm_gate", "glm_gate_ln", "qk",
-                            "gelu_bf16", "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms", "temb", "fp8", "wan_ln"],
+                            "gelu_bf16", "gelu_fp16", "rms", "rms_tok", "gate_rms_tok", "qk_rms", "temb", "fp8", "wan_ln",
+                            "copy_sana"],
                    help="workload timed as the headline (profiling runs); the JSON line's metric "
                         "and roofline describe the Sana LN+modulate only when this is 'sana'")
     args = p.parse_args()

@@ -87,7 +87,7 @@ def test_non_finite_rows(ad):
 
 
 def test_flux_like_shape_sampled_rows(ad):
-    case(ad, 1, 4608, 3072, 0.03, seed=11, rows=range(0, 4608, 5), expect="rows")
+    case(ad, 1, 4608, 3072, 0.03, seed=11, expect="rows")
 
 
 @pytest.mark.parametrize("D", [3072, 2240])

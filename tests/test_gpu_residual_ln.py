@@ -36,7 +36,7 @@ def case(ad, B, N, D, dtype="bf16", seed=0, gate_b=True, in_place=None, rows=Non
 
 
 def test_glm_shape(ad):
-    case(ad, 1, 4096, 4096, rows=range(0, 4096, 3))
+    case(ad, 1, 4096, 4096)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
