@@ -102,6 +102,12 @@ ln_rows_kernel(const RowsParams p) {
                 prefetch_l2(p.x + b0 * p.sxB + n0 * p.sxN, (uint64_t)p.D * 2);
             }
         }
+        // and the scale / shift rows the shared table is built from
+        if (threadIdx.x < 2 * p.B && threadIdx.x < 64) {
+            const int64_t bb = threadIdx.x >> 1;
+            prefetch_l2((threadIdx.x & 1) ? p.shift + bb * p.s_shift_b : p.scale + bb * p.s_scale_b,
+                        (uint64_t)p.D * 2);
+        }
     }
     pdl_wait();
     pdl_trigger();
