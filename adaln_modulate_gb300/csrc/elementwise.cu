@@ -57,15 +57,16 @@ gate_add_kernel(uint16_t *out, const uint16_t *x, const uint16_t *gate, int64_t 
             prefetch_l2(y + e0, (uint64_t)(e1 - e0) * 2);
         }
     }
-    pdl_wait();
-    pdl_trigger();
     constexpr int R = EPT / 2;
     const int64_t stride = (int64_t)gridDim.x * kEwThreads;
     // sample b and column col of the thread's element, advanced by the
-    // grid step with a carry (no division per iteration)
+    // grid step with a carry (no division per iteration); the divisions
+    // depend on launch parameters only and are done before the wait
     const int64_t v0 = (int64_t)blockIdx.x * kEwThreads + threadIdx.x, step = stride * EPT;
     const int64_t qb = step / ND, rb = step - qb * ND, rc = step % D;
     int64_t b = v0 * EPT / ND, in_b = v0 * EPT - b * ND, col = v0 * EPT % D;
+    pdl_wait();
+    pdl_trigger();
     for (int64_t v = v0; v < nvec; v += stride) {
         const int64_t e0 = v * EPT;
         uint32_t xr[R], yr[R], gr[R], o[R];

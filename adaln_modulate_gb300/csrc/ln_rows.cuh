@@ -109,10 +109,9 @@ ln_rows_kernel(const RowsParams p) {
                         (uint64_t)p.D * 2);
         }
     }
-    pdl_wait();
-    pdl_trigger();
-    QuantE4M3 qc{};  // E4M3: the static scale (written by earlier work on the stream) and its constants
-    if constexpr (E4M3) qc = quant_setup<T>(*p.qscale);
+    // Everything below up to the wait depends on launch parameters only; the
+    // first row's loads are the first thing after it (a 64-bit division or a
+    // parameter read there delays every row of the call).
     const int u = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int D = p.D;
@@ -140,8 +139,8 @@ ln_rows_kernel(const RowsParams p) {
 
     // xv[i][s] = the 4 elements of lane l0 + 8s at step i (2 registers)
     uint32_t xv[NI][4][2];
-    auto load_row = [&](int64_t b, int64_t n) {
-        const uint16_t *xr = p.x + b * p.sxB + n * p.sxN + c0;
+    auto row_x = [&](int64_t b, int64_t n) { return p.x + b * p.sxB + n * p.sxN + c0; };
+    auto load_row = [&](const uint16_t *xr) {
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
 #pragma unroll
@@ -166,7 +165,14 @@ ln_rows_kernel(const RowsParams p) {
             n -= q * N;
         }
     };
-    if (row < r1) load_row(rb, rn);
+    const uint16_t *const x_first = row_x(rb, rn);
+    pdl_wait();
+    pdl_trigger();
+    if (row < r1) load_row(x_first);
+    // E4M3: the static scale (written by earlier work on the stream) and its
+    // constants, once the first row is on its way
+    QuantE4M3 qc{};
+    if constexpr (E4M3) qc = quant_setup<T>(*p.qscale);
 
     if constexpr (OPSH) {
         // all loads of a batch in flight before any is used
@@ -338,7 +344,7 @@ ln_rows_kernel(const RowsParams p) {
                 }
             }
         }
-        if (row + kRowsThreads / 32 < r1) load_row(bn, nn);
+        if (row + kRowsThreads / 32 < r1) load_row(row_x(bn, nn));
         rb = bn;
         rn = nn;
     }

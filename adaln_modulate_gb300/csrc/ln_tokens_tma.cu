@@ -109,18 +109,25 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
     const uint32_t my_s = tile_s + (uint32_t)(kTTRowBytes * l + 16 * h);  // (step 0, e 0) of this thread
 
     // Launch parameters are not data of the previous kernel: read them, fetch
-    // the tensor map's descriptor and set up the barriers before waiting on
-    // that kernel (the first read of a parameter misses the constant cache,
-    // about a microsecond).  The first tile's coordinates go through shared
-    // memory so that the parameter reads stay ahead of the wait.
+    // the tensor map's descriptor, set up the barriers and arm them with the
+    // first tile's byte counts before waiting on that kernel (the first read
+    // of a parameter misses the constant cache, about a microsecond; an armed
+    // phase still completes only once its bytes have arrived).  Thread 0
+    // keeps the first tile's coordinates in registers and issues its loads
+    // as the first thing after the wait (anything ahead of them there, such
+    // as a parameter read or a 64-bit division, delays the whole landing);
+    // the other threads take the coordinates from shared memory.
     __shared__ int64_t first_tile[2];
+    int b0 = 0, f0 = 0;  // the first tile (thread 0)
     if (tid == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
 #pragma unroll
         for (int i = 0; i < NI; ++i) mbar_init(bar_s + 8 * i, 1);
+#pragma unroll
+        for (int i = 0; i < NI; ++i) mbar_expect_tx(bar_s + 8 * i, (uint32_t)kStepBytes);
         asm volatile("fence.mbarrier_init.release.cluster;\nfence.proxy.async.shared::cta;" ::: "memory");
-        const int64_t b0 = (int64_t)blockIdx.x / tiles_per_b;
-        const int64_t f0 = ((int64_t)blockIdx.x - b0 * tiles_per_b) * kTT;
+        b0 = (int)((int64_t)blockIdx.x / tiles_per_b);
+        f0 = (int)(((int64_t)blockIdx.x - (int64_t)b0 * tiles_per_b) * kTT);
         first_tile[0] = b0;
         first_tile[1] = f0;
         // Ask L2 for the first tile and its sample's scale / shift rows now,
@@ -129,12 +136,19 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
         // SM's accesses to global memory meet, so the loads issued after the
         // wait still see everything the previous kernel wrote.
 #pragma unroll
-        for (int i = 0; i < NI; ++i) tma_prefetch_4d(&tmx, (int)f0, 128 * i, 0, (int)b0);
+        for (int i = 0; i < NI; ++i) tma_prefetch_4d(&tmx, f0, 128 * i, 0, b0);
         prefetch_l2(scale + b0 * s_scale_b, (uint64_t)D * 2);
         prefetch_l2(shift + b0 * s_shift_b, (uint64_t)D * 2);
     }
     __syncthreads();
     pdl_wait();
+    if (tid == 0) {
+        // the first tile's loads, from one thread in box order (boxes issued
+        // by several warps at once land interleaved, the first one late)
+#pragma unroll
+        for (int i = 0; i < NI; ++i)
+            tma_load_4d(tile_s + (uint32_t)(i * kStepBytes), &tmx, f0, 128 * i, 0, b0, bar_s + 8 * i);
+    }
     pdl_trigger();
 
     int64_t table_b = -1;
@@ -147,13 +161,15 @@ ln_tokens_tma_kernel(const __grid_constant__ CUtensorMap tmx, uint16_t *out, int
         }
 
         if (tid == 0) {
-            // the previous tile's shared reads are ordered before these
-            // asynchronous writes by the barrier that ended it
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (t != blockIdx.x) {
+                // the previous tile's shared reads are ordered before these
+                // asynchronous writes by the barrier that ended it
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
-            for (int i = 0; i < NI; ++i) {
-                mbar_expect_tx(bar_s + 8 * i, (uint32_t)kStepBytes);
-                tma_load_4d(tile_s + (uint32_t)(i * kStepBytes), &tmx, (int)n0, 128 * i, 0, (int)b, bar_s + 8 * i);
+                for (int i = 0; i < NI; ++i) {
+                    mbar_expect_tx(bar_s + 8 * i, (uint32_t)kStepBytes);
+                    tma_load_4d(tile_s + (uint32_t)(i * kStepBytes), &tmx, (int)n0, 128 * i, 0, (int)b, bar_s + 8 * i);
+                }
             }
             const int64_t tn = t + gridDim.x;
             if (tn < ntiles) {

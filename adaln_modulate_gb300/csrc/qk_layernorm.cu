@@ -55,8 +55,26 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
     __shared__ __align__(16) float aff[2][2][128];  // [q / k][w / b][column]
     const int nl = NL ? NL : (Dh >> 2);
     const float Df = (float)Dh;
+    const int64_t total = rows_q + rows_k;
+    const int64_t r_first = (int64_t)blockIdx.x * kQkThreads + threadIdx.x;
+
+    uint32_t v[32][2];  // lane l: elements 4l..4l+3
+    auto load_row = [&](int64_t r) {
+        const uint16_t *src = r < rows_q ? q + r * Dh : k + (r - rows_q) * Dh;
+#pragma unroll
+        for (int l = 0; l < 32; ++l) {
+            if (l < nl) {
+                ld_stream8(v[l], src + 4 * l);
+            } else {
+                v[l][0] = v[l][1] = 0u;
+            }
+        }
+    };
+    // the thread's first row goes out first after the wait; the affine
+    // parameters (needed only for the output) follow
     pdl_wait();
     pdl_trigger();
+    if (r_first < total) load_row(r_first);
     for (int c = threadIdx.x; c < 128; c += kQkThreads) {
         const bool in = c < Dh;
         aff[0][0][c] = (in && rows_q) ? h_f32<T>(wq[c]) : 0.0f;
@@ -66,24 +84,12 @@ qk_ln_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *k_out
     }
     __syncthreads();
 
-    const int64_t total = rows_q + rows_k;
-    for (int64_t r = (int64_t)blockIdx.x * kQkThreads + threadIdx.x; r < total;
-         r += (int64_t)gridDim.x * kQkThreads) {
+    for (int64_t r = r_first; r < total; r += (int64_t)gridDim.x * kQkThreads) {
         const bool isq = r < rows_q;
-        const uint16_t *src = isq ? q + r * Dh : k + (r - rows_q) * Dh;
         uint16_t *dst = isq ? q_out + r * Dh : k_out + (r - rows_q) * Dh;
         const float *w = aff[isq ? 0 : 1][0];
         const float *bb = aff[isq ? 0 : 1][1];
-
-        uint32_t v[32][2];  // lane l: elements 4l..4l+3
-#pragma unroll
-        for (int l = 0; l < 32; ++l) {
-            if (l < nl) {
-                ld_stream8(v[l], src + 4 * l);
-            } else {
-                v[l][0] = v[l][1] = 0u;
-            }
-        }
+        if (r != r_first) load_row(r);
 
         // Welford of every lane (counts 1..4) on lane pairs (2k, 2k+1);
         // lanes at or past nl keep (0, 0).  RMS: the sums of squares in qq
@@ -225,8 +231,31 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
         const int64_t ks = nb > rows_q ? nb : rows_q;
         if (ne > ks) prefetch_l2(k + (ks - rows_q) * 128, (uint64_t)(ne - ks) * 256);
     }
+    const int t = threadIdx.x & 1;
+    const int64_t total = rows_q + rows_k;
+    const int64_t w0 = (((int64_t)blockIdx.x * kQkThreads + threadIdx.x) >> 5) * 16;
+    const int64_t wstride = ((int64_t)gridDim.x * kQkThreads >> 5) * 16;
+    const int rin = (threadIdx.x & 31) >> 1;  // row of this thread within the warp's 16
+
+    uint32_t v[8][4];  // k: lanes 4k + 2t (v[k][0..1]) and 4k + 2t + 1 (v[k][2..3])
+    auto load_rows = [&](int64_t r) {
+        const uint16_t *src = r < rows_q ? q + r * 128 : k + (r - rows_q) * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            if (r < total) {
+                asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v[kk][0]), "=r"(v[kk][1]), "=r"(v[kk][2]), "=r"(v[kk][3])
+                             : "l"(src + 16 * kk + 8 * t));
+            } else {
+                v[kk][0] = v[kk][1] = v[kk][2] = v[kk][3] = 0u;
+            }
+        }
+    };
+    // the warp's first 16 rows go out first after the wait; the affine
+    // parameters (needed only for the output) follow
     pdl_wait();
     pdl_trigger();
+    load_rows(w0 + rin);
     for (int c = threadIdx.x; c < 128; c += kQkThreads) {
         aff[0][0][c] = rows_q ? h_f32<T>(wq[c]) : 0.0f;
         aff[0][1][c] = (!RMS && rows_q) ? h_f32<T>(bq[c]) : 0.0f;
@@ -235,32 +264,14 @@ qk_ln_pair_kernel(uint16_t *q_out, const uint16_t *q, int64_t rows_q, uint16_t *
     }
     __syncthreads();
 
-    const int t = threadIdx.x & 1;
-    const int64_t total = rows_q + rows_k;
-    const int64_t w0 = (((int64_t)blockIdx.x * kQkThreads + threadIdx.x) >> 5) * 16;
-    const int64_t wstride = ((int64_t)gridDim.x * kQkThreads >> 5) * 16;
-    const int rin = (threadIdx.x & 31) >> 1;  // row of this thread within the warp's 16
-
     for (int64_t rbase = w0; rbase < total; rbase += wstride) {
         const int64_t r = rbase + rin;
         const bool active = r < total;
         const bool isq = r < rows_q;
-        const uint16_t *src = isq ? q + r * 128 : k + (r - rows_q) * 128;
         uint16_t *dst = isq ? q_out + r * 128 : k_out + (r - rows_q) * 128;
         const float *w = aff[isq ? 0 : 1][0];
         const float *bb = aff[isq ? 0 : 1][1];
-
-        uint32_t v[8][4];  // k: lanes 4k + 2t (v[k][0..1]) and 4k + 2t + 1 (v[k][2..3])
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            if (active) {
-                asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(v[kk][0]), "=r"(v[kk][1]), "=r"(v[kk][2]), "=r"(v[kk][3])
-                             : "l"(src + 16 * kk + 8 * t));
-            } else {
-                v[kk][0] = v[kk][1] = v[kk][2] = v[kk][3] = 0u;
-            }
-        }
+        if (rbase != w0) load_rows(r);
 
         // Welford of lane pair (4k + 2t, 4k + 2t + 1), one f32x2 chain per k
         // (RMS: the sums of squares in qq)

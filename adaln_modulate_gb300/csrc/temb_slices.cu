@@ -56,8 +56,6 @@ template <int TDT, int EDT, bool VEC>
 __global__ void __launch_bounds__(kTembThreads)
 temb_slices_kernel(float *__restrict__ out, int64_t s_out_k, const void *__restrict__ table,
                    const void *__restrict__ temb, int64_t BS, int64_t K, int64_t D) {
-    pdl_wait();
-    pdl_trigger();
     const int64_t W = VEC ? D / 8 : D;  // units per (token, chunk) row
     const int64_t total = BS * K * W;
     const int64_t stride = (int64_t)gridDim.x * kTembThreads;
@@ -69,6 +67,9 @@ temb_slices_kernel(float *__restrict__ out, int64_t s_out_k, const void *__restr
     const int64_t qs1 = (qr + 1) / K, rk1 = (qr + 1) - qs1 * K;  // a step of qr + 1 rows
     int64_t row0 = u0 / W, w = u0 - row0 * W;
     int64_t bs = row0 / K, k = row0 - bs * K;
+    // (the divisions above depend on launch parameters only)
+    pdl_wait();
+    pdl_trigger();
     for (int64_t u = u0; u < total; u += stride) {
         const int64_t row = bs * K + k;
         if constexpr (VEC) {
