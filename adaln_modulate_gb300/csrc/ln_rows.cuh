@@ -6,6 +6,8 @@
 #include "ln_common.cuh"
 #include "quant_e4m3.cuh"
 
+#include <type_traits>
+
 namespace adaln {
 
 // ---------------------------------------------------------------------
@@ -308,41 +310,54 @@ ln_rows_kernel(const RowsParams p) {
         uint16_t *orow = p.out + row * (int64_t)D + c0;
         uint8_t *orow8 = reinterpret_cast<uint8_t *>(p.out) + row * (int64_t)D + c0;  // E4M3
         const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
+        // (e4m3: two copies of the pass, the quantiser chosen once per row;
+        // a choice per chunk inside the unrolled loop is much slower)
+        auto pass2 = [&](auto fastq) {
 #pragma unroll
-        for (int i = 0; i < NI; ++i) {
+            for (int i = 0; i < NI; ++i) {
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                if (i < NI - 1 || vlast[s]) {
-                    const int off = 512 * i + 32 * s;
-                    uint32_t op[2], sh[2], o[2];
-                    if constexpr (OPSH) {
-                        const uint4 t = *reinterpret_cast<const uint4 *>(ob + off);
-                        op[0] = t.x;
-                        sh[0] = t.y;
-                        op[1] = t.z;
-                        sh[1] = t.w;
-                    } else {
-                        uint32_t sc[2];
-                        ld_keep8(sc, scr + off);
-                        ld_keep8(sh, shr + off);
-                        op[0] = add16x2<T>(sc[0], one16x2<T>());
-                        op[1] = add16x2<T>(sc[1], one16x2<T>());
-                    }
+                for (int s = 0; s < 4; ++s) {
+                    if (i < NI - 1 || vlast[s]) {
+                        const int off = 512 * i + 32 * s;
+                        uint32_t op[2], sh[2], o[2];
+                        if constexpr (OPSH) {
+                            const uint4 t = *reinterpret_cast<const uint4 *>(ob + off);
+                            op[0] = t.x;
+                            sh[0] = t.y;
+                            op[1] = t.z;
+                            sh[1] = t.w;
+                        } else {
+                            uint32_t sc[2];
+                            ld_keep8(sc, scr + off);
+                            ld_keep8(sh, shr + off);
+                            op[0] = add16x2<T>(sc[0], one16x2<T>());
+                            op[1] = add16x2<T>(sc[1], one16x2<T>());
+                        }
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        float xl, xh;
-                        unpack_again<T>(xv[i][s][k], xl, xh);
-                        float y0, y1;
-                        f2_split(f2_mul(f2_sub(f2(xl, xh), mm), rr), y0, y1);
-                        o[k] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0, y1), op[k]), sh[k]);
-                    }
-                    if constexpr (E4M3) {
-                        st4(orow8 + off, quant4_e4m3<T>(o, qc));
-                    } else {
-                        st8(orow + off, o);
+                        for (int k = 0; k < 2; ++k) {
+                            float xl, xh;
+                            unpack_again<T>(xv[i][s][k], xl, xh);
+                            float y0, y1;
+                            f2_split(f2_mul(f2_sub(f2(xl, xh), mm), rr), y0, y1);
+                            o[k] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0, y1), op[k]), sh[k]);
+                        }
+                        if constexpr (E4M3) {
+                            if constexpr (decltype(fastq)::value) {
+                                st4(orow8 + off, quant4_e4m3_fast<T>(o, qc));
+                            } else {
+                                st4(orow8 + off, quant4_e4m3_window<T>(o, qc));
+                            }
+                        } else {
+                            st8(orow + off, o);
+                        }
                     }
                 }
             }
+        };
+        if (E4M3 && qc.fast) {
+            pass2(std::true_type{});
+        } else {
+            pass2(std::false_type{});
         }
         if (row + kRowsThreads / 32 < r1) load_row(row_x(bn, nn));
         rb = bn;

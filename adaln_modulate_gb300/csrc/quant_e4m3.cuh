@@ -33,9 +33,24 @@ __device__ __forceinline__ float div_by_recip(float a, float b, float r) {
 // magnitudes against it with one packed min, one max and two compares,
 // runs the correction on f32x2 pairs when they all fit, and takes the exact
 // quotient one value at a time (zeros, NaN, extreme magnitudes) otherwise.
+//
+// For an ordinary positive scale (2^-60 <= qs <= 2^60, and the window's
+// upper bound at least 1024 qs) a branch-free form (quant4_e4m3_fast) gives
+// the same codes: each value's magnitude is clamped to the window's upper
+// bound (every |y| above it saturates to 448 either way) and its sign flipped
+// in one packed min.NaN.xorsign.abs with the negated bound, and the
+// correction runs on -y:
+// q = RN(y r), e' = RN(q qs - y) = -e, q' = RN(q - e' r), the same values as
+// above, but with zeros that keep their sign (RN(q + e r) turns -0 into +0).
+// Below the window's lower bound the correction may be inexact, but there
+// |y / qs| < 2^-40: the code is a signed zero either way, and the sign comes
+// out right (q is RN(y r) or carries its sign).  Infinities become the
+// clamped bound (saturating), NaN stays NaN.
 struct QuantE4M3 {
     float qs, qr, nqs;  // the scale, RN(1 / scale), -scale
     uint32_t lo2, hi2;  // the pattern window, in both 16-bit halves
+    uint32_t nhi2;      // the upper bound's pattern with the sign bit set, in both halves
+    bool fast;          // the scale is ordinary and positive: quant4_e4m3_fast applies
 };
 
 template <DT T> __device__ __forceinline__ uint32_t pattern_ceil(float t);
@@ -49,6 +64,11 @@ template <> __device__ __forceinline__ uint32_t pattern_ceil<DT::FP16>(float t) 
 }
 template <> __device__ __forceinline__ uint32_t pattern_floor<DT::FP16>(float t) {
     return __half_as_ushort(__float2half_rd(t));
+}
+template <DT T> __device__ __forceinline__ float pattern_value(uint32_t p);
+template <> __device__ __forceinline__ float pattern_value<DT::BF16>(uint32_t p) { return __uint_as_float(p << 16); }
+template <> __device__ __forceinline__ float pattern_value<DT::FP16>(uint32_t p) {
+    return __half2float(__ushort_as_half((unsigned short)p));
 }
 
 template <DT T>
@@ -67,6 +87,10 @@ __device__ __forceinline__ QuantE4M3 quant_setup(float qs) {
     }
     c.lo2 = lp | (lp << 16);
     c.hi2 = hp | (hp << 16);
+    // (false for NaN and every negative scale; an fp16 bound of 65504 needs qs <= 63.97)
+    c.fast = qs >= 0x1p-60f && qs <= 0x1p+60f && pattern_value<T>(hp) >= 1024.0f * qs;
+    const uint32_t nh = (c.fast ? hp : 0u) | 0x8000u;
+    c.nhi2 = nh | (nh << 16);
     return c;
 }
 
@@ -93,9 +117,42 @@ template <> __device__ __forceinline__ bool window4<DT::FP16>(uint32_t m0, uint3
            __hbge2(__hmin2(a, b), *reinterpret_cast<const __half2 *>(&lo2));
 }
 
-// the e4m3 codes of 4 storage values (2 packed pairs), in memory order
+// -clamp(y) of a packed pair: min(|y|, |b|) with the sign of y flipped (b
+// negative), NaN kept
+template <DT T> __device__ __forceinline__ uint32_t neg_clamp16x2(uint32_t y, uint32_t nb);
+template <> __device__ __forceinline__ uint32_t neg_clamp16x2<DT::BF16>(uint32_t y, uint32_t nb) {
+    uint32_t r;
+    asm("min.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(nb));
+    return r;
+}
+template <> __device__ __forceinline__ uint32_t neg_clamp16x2<DT::FP16>(uint32_t y, uint32_t nb) {
+    uint32_t r;
+    asm("min.NaN.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(nb));
+    return r;
+}
+
+// the e4m3 codes of 4 storage values (2 packed pairs), in memory order, for
+// an ordinary positive scale (c.fast): no branch
 template <DT T>
-__device__ __forceinline__ uint32_t quant4_e4m3(const uint32_t *o, const QuantE4M3 &c) {
+__device__ __forceinline__ uint32_t quant4_e4m3_fast(const uint32_t *o, const QuantE4M3 &c) {
+    const uint32_t n0 = neg_clamp16x2<T>(o[0], c.nhi2), n1 = neg_clamp16x2<T>(o[1], c.nhi2);
+    const f2_t a01 = f2(lo_f32<T>(n0), hi_f32<T>(n0)), a23 = f2(lo_f32<T>(n1), hi_f32<T>(n1));  // -y
+    const f2_t nr2 = f2(-c.qr, -c.qr), s2 = f2(c.qs, c.qs);
+    f2_t p01 = f2_mul(a01, nr2), p23 = f2_mul(a23, nr2);  // RN(y r)
+    p01 = f2_fma(f2_fma(p01, s2, a01), nr2, p01);         // q - (q s - y) r
+    p23 = f2_fma(f2_fma(p23, s2, a23), nr2, p23);
+    float q0, q1, q2, q3;
+    f2_split(p01, q0, q1);
+    f2_split(p23, q2, q3);
+    const uint32_t q01 = __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t q23 = __nv_cvt_float2_to_fp8x2(make_float2(q2, q3), __NV_SATFINITE, __NV_E4M3);
+    return (q01 & 0xffffu) | (q23 << 16);
+}
+
+// the e4m3 codes of 4 storage values (2 packed pairs), in memory order, for
+// any scale: the window check, the correction, the exact quotient outside
+template <DT T>
+__device__ __forceinline__ uint32_t quant4_e4m3_window(const uint32_t *o, const QuantE4M3 &c) {
     float q0, q1, q2, q3;
     if (window4<T>(o[0] & 0x7fff7fffu, o[1] & 0x7fff7fffu, c.lo2, c.hi2)) {
         const f2_t a01 = f2(lo_f32<T>(o[0]), hi_f32<T>(o[0])), a23 = f2(lo_f32<T>(o[1]), hi_f32<T>(o[1]));
@@ -116,6 +173,11 @@ __device__ __forceinline__ uint32_t quant4_e4m3(const uint32_t *o, const QuantE4
     const uint32_t q01 = __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3);
     const uint32_t q23 = __nv_cvt_float2_to_fp8x2(make_float2(q2, q3), __NV_SATFINITE, __NV_E4M3);
     return (q01 & 0xffffu) | (q23 << 16);
+}
+
+template <DT T>
+__device__ __forceinline__ uint32_t quant4_e4m3(const uint32_t *o, const QuantE4M3 &c) {
+    return c.fast ? quant4_e4m3_fast<T>(o, c) : quant4_e4m3_window<T>(o, c);
 }
 
 }  // namespace adaln

@@ -28,7 +28,8 @@ def helper(tmp_path_factory):
                     "-fmad=false", "-shared", os.path.join(HERE, "cuda", "div_sweep.cu"), "-o", so], check=True)
     lib = ctypes.CDLL(so)
     lib.div_sweep.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong]
-    lib.quant4_sweep.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int]
+    lib.quant4_sweep.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int,
+                                 ctypes.c_int, ctypes.c_void_p]
     return lib
 
 
@@ -64,18 +65,35 @@ def _tie_scales():
     return [3.0, 5.0, 7.0, 11.0, 13.0, 0.375, 0.625]
 
 
+def _extreme_scales():
+    # outside the branch-free form's range (2^-60 .. 2^60, positive) or, for
+    # fp16, above 63.97 (65504 / 1024): the window form only
+    return [2.0 ** -70, 2.0 ** 70, -0.03, -3.0, 100.0, 3.0e4]
+
+
+@pytest.mark.parametrize("window", [0, 1], ids=["as_picked", "window_form"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-def test_quantiser_codes_equal_the_oracle(helper, dtype):
-    """The rows kernel's 4-wide quantiser (the product with RN(1/s) and the
-    exact quotient near e4m3 boundaries) against the oracle's IEEE division
-    and e4m3 encoder, for every 16-bit pattern (NaN codes compared as NaN)."""
+def test_quantiser_codes_equal_the_oracle(helper, dtype, window):
+    """The rows kernel's 4-wide quantisers against the oracle's IEEE division
+    and e4m3 encoder, for every 16-bit pattern (NaN codes compared as NaN):
+    the form the kernel picks for each scale (the branch-free one: clamped
+    magnitudes and the correction on -y; or the window form: the product with
+    RN(1/s) and the exact quotient near e4m3 boundaries), and the window form
+    forced for every scale."""
     pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     yg = torch.from_numpy(pats.view(np.int16).copy()).cuda()
     codes = torch.empty(65536, dtype=torch.uint8, device="cuda")
-    for s in _scales() + _tie_scales():
-        assert helper.quant4_sweep(yg.data_ptr(), s, codes.data_ptr(), 65536 // 4, int(dtype == "fp16")) == 0
+    fast = torch.zeros(1, dtype=torch.int32, device="cuda")
+    picked = set()
+    for s in _scales() + _tie_scales() + _extreme_scales():
+        assert helper.quant4_sweep(yg.data_ptr(), s, codes.data_ptr(), 65536 // 4, int(dtype == "fp16"), window,
+                                   fast.data_ptr()) == 0
+        expect_fast = 2.0 ** -60 <= s <= 2.0 ** 60 and (dtype == "bf16" or s <= 65504.0 / 1024.0)
+        assert bool(fast.item()) == expect_fast, s
+        picked.add(expect_fast and not window)
         got = codes.cpu().numpy()
         ref = oracle.quant_e4m3(pats, s, dtype)
         nan_r = (ref & 0x7F) == 0x7F
         assert np.array_equal((got & 0x7F) == 0x7F, nan_r), s
         assert np.array_equal(got[~nan_r], ref[~nan_r]), (s, int((got[~nan_r] != ref[~nan_r]).sum()))
+    assert picked == ({True, False} if not window else {False})
