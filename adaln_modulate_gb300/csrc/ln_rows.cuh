@@ -171,10 +171,29 @@ ln_rows_kernel(const RowsParams p) {
     pdl_wait();
     pdl_trigger();
     if (row < r1) load_row(x_first);
-    // E4M3: the static scale (written by earlier work on the stream) and its
-    // constants, once the first row is on its way
+    // E4M3: the static scale (written by earlier work on the stream) and the
+    // device's memo of the plain-product search, read once the first row is
+    // on its way; the constants are computed while the table's loads are in
+    // flight, the form is picked after the barrier that ends the table
+    float qs_in = 0.0f;
+    unsigned long long memo = 0;
+    __shared__ unsigned long long memo_s;
+    if constexpr (E4M3) {
+        qs_in = *p.qscale;
+        memo = plain_memo_load<T>();
+    }
     QuantE4M3 qc{};
-    if constexpr (E4M3) qc = quant_setup<T>(*p.qscale);
+    auto quant_prepare = [&] {
+        if constexpr (E4M3) {
+            qc = quant_setup<T>(qs_in);
+            if (threadIdx.x == 0) memo_s = memo;
+        }
+    };
+    if constexpr (E4M3 && !OPSH) {
+        quant_prepare();
+        __syncthreads();
+        quant_pick_plain<T>(qc, &memo_s, threadIdx.x, kRowsThreads);
+    }
 
     if constexpr (OPSH) {
         // all loads of a batch in flight before any is used
@@ -193,6 +212,7 @@ ln_rows_kernel(const RowsParams p) {
                         asm("ld.global.nc.b32 %0, [%1];" : "=r"(g2[k]) : "l"(p.gate + bb * p.s_gate_b + 2 * cp));
                 }
             }
+            if (base == 0) quant_prepare();
 #pragma unroll
             for (int k = 0; k < kFill; ++k) {
                 const int e = base + k * kRowsThreads + threadIdx.x;
@@ -204,115 +224,116 @@ ln_rows_kernel(const RowsParams p) {
             }
         }
         __syncthreads();
+        if constexpr (E4M3) quant_pick_plain<T>(qc, &memo_s, threadIdx.x, kRowsThreads);
     }
 
-    for (; row < r1; row += kRowsThreads / 32) {
-        const int64_t b = rb, n = rn;
-        int64_t bn = rb, nn = rn;  // the warp's next row
-        next_bn(bn, nn);
+    // the row loop, one copy per e4m3 quantiser form (chosen once per CTA;
+    // a choice per row or per chunk inside one loop is slower)
+    auto row_loop = [&](auto qform) {
+        for (; row < r1; row += kRowsThreads / 32) {
+            const int64_t b = rb, n = rn;
+            int64_t bn = rb, nn = rn;  // the warp's next row
+            next_bn(bn, nn);
 
-        // pass 1: Welford (or the sum of squares) of lanes (s0, s1) and
-        // (s2, s3), one f32x2 op each
-        f2_t m01 = f2(0.f, 0.f), q01 = m01, m23 = m01, q23 = m01;
-        const uint16_t *gr = nullptr;  // GATE: this row's gate row (or value)
-        uint32_t gs = 0;               // GATE_SCALAR: the value in both halves
-        if constexpr (GATE) gr = p.gate + b * p.s_gate_b + n * p.s_gate_n;
-        if constexpr (GM == GATE_SCALAR) {
-            const uint32_t g1 = ldg_u16(gr);
-            gs = g1 | (g1 << 16);
-        }
-        static_for<0, NI>([&](auto I) {
-            constexpr int i = decltype(I)::value;
-            if constexpr (GATE) {
-                // this step's chunks become r = round(x + round(gate * y)), stored
-                const uint16_t *yr = p.y + row * (int64_t)D + c0;
-                uint16_t *rr_out = p.r_out + row * (int64_t)D + c0;
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    if (i < NI - 1 || vlast[s]) {
-                        const int off = 512 * i + 32 * s;
-                        uint32_t yv[2], gv[2];
-                        ld_stream8(yv, yr + off);
-                        if constexpr (GM == GATE_SCALAR) {
-                            gv[0] = gv[1] = gs;
-                        } else if constexpr (GTAB) {
-                            const uint2 t = *reinterpret_cast<const uint2 *>(opsh + 2 * (int)(p.B * (D / 2)) + b * (D / 2) + (c0 + off) / 2);
-                            gv[0] = t.x;
-                            gv[1] = t.y;
-                        } else {
-                            ld_keep8(gv, gr + c0 + off);
-                        }
-                        xv[i][s][0] = add16x2<T>(xv[i][s][0], mul16x2<T>(gv[0], yv[0]));
-                        xv[i][s][1] = add16x2<T>(xv[i][s][1], mul16x2<T>(gv[1], yv[1]));
-                        st8(rr_out + off, xv[i][s]);
-                    }
-                }
+            // pass 1: Welford (or the sum of squares) of lanes (s0, s1) and
+            // (s2, s3), one f32x2 op each
+            f2_t m01 = f2(0.f, 0.f), q01 = m01, m23 = m01, q23 = m01;
+            const uint16_t *gr = nullptr;  // GATE: this row's gate row (or value)
+            uint32_t gs = 0;               // GATE_SCALAR: the value in both halves
+            if constexpr (GATE) gr = p.gate + b * p.s_gate_b + n * p.s_gate_n;
+            if constexpr (GM == GATE_SCALAR) {
+                const uint32_t g1 = ldg_u16(gr);
+                gs = g1 | (g1 << 16);
             }
-            static_for<0, 4>([&](auto E) {
-                constexpr int e = decltype(E)::value;
-                [[maybe_unused]] constexpr float r = Rcp<4 * i + e + 1>::value;  // Welford 1/(count+1)
-                float a[4];
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    a[s] = (e & 1) ? hi_f32<T>(xv[i][s][e >> 1]) : lo_f32<T>(xv[i][s][e >> 1]);
-                if constexpr (RMS) {
-                    // masked tail lanes hold zeros: adding 0 * 0 keeps the sum
-                    const f2_t a01 = f2(a[0], a[1]), a23 = f2(a[2], a[3]);
-                    q01 = f2_add(q01, f2_mul(a01, a01));
-                    q23 = f2_add(q23, f2_mul(a23, a23));
-                } else if (!TAIL || i < NI - 1) {
-                    push2(m01, q01, f2(a[0], a[1]), r);
-                    push2(m23, q23, f2(a[2], a[3]), r);
-                } else {
-                    // last step with masked lanes: keep the old state there
-                    f2_t nm01 = m01, nq01 = q01, nm23 = m23, nq23 = q23;
-                    push2(nm01, nq01, f2(a[0], a[1]), r);
-                    push2(nm23, nq23, f2(a[2], a[3]), r);
-                    float o[4], w[4], oq[4], wq[4];
-                    f2_split(m01, o[0], o[1]);
-                    f2_split(m23, o[2], o[3]);
-                    f2_split(nm01, w[0], w[1]);
-                    f2_split(nm23, w[2], w[3]);
-                    f2_split(q01, oq[0], oq[1]);
-                    f2_split(q23, oq[2], oq[3]);
-                    f2_split(nq01, wq[0], wq[1]);
-                    f2_split(nq23, wq[2], wq[3]);
+            static_for<0, NI>([&](auto I) {
+                constexpr int i = decltype(I)::value;
+                if constexpr (GATE) {
+                    // this step's chunks become r = round(x + round(gate * y)), stored
+                    const uint16_t *yr = p.y + row * (int64_t)D + c0;
+                    uint16_t *rr_out = p.r_out + row * (int64_t)D + c0;
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        o[s] = vlast[s] ? w[s] : o[s];
-                        oq[s] = vlast[s] ? wq[s] : oq[s];
+                        if (i < NI - 1 || vlast[s]) {
+                            const int off = 512 * i + 32 * s;
+                            uint32_t yv[2], gv[2];
+                            ld_stream8(yv, yr + off);
+                            if constexpr (GM == GATE_SCALAR) {
+                                gv[0] = gv[1] = gs;
+                            } else if constexpr (GTAB) {
+                                const uint2 t = *reinterpret_cast<const uint2 *>(opsh + 2 * (int)(p.B * (D / 2)) + b * (D / 2) + (c0 + off) / 2);
+                                gv[0] = t.x;
+                                gv[1] = t.y;
+                            } else {
+                                ld_keep8(gv, gr + c0 + off);
+                            }
+                            xv[i][s][0] = add16x2<T>(xv[i][s][0], mul16x2<T>(gv[0], yv[0]));
+                            xv[i][s][1] = add16x2<T>(xv[i][s][1], mul16x2<T>(gv[1], yv[1]));
+                            st8(rr_out + off, xv[i][s]);
+                        }
                     }
-                    m01 = f2(o[0], o[1]);
-                    m23 = f2(o[2], o[3]);
-                    q01 = f2(oq[0], oq[1]);
-                    q23 = f2(oq[2], oq[3]);
                 }
+                static_for<0, 4>([&](auto E) {
+                    constexpr int e = decltype(E)::value;
+                    [[maybe_unused]] constexpr float r = Rcp<4 * i + e + 1>::value;  // Welford 1/(count+1)
+                    float a[4];
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        a[s] = (e & 1) ? hi_f32<T>(xv[i][s][e >> 1]) : lo_f32<T>(xv[i][s][e >> 1]);
+                    if constexpr (RMS) {
+                        // masked tail lanes hold zeros: adding 0 * 0 keeps the sum
+                        const f2_t a01 = f2(a[0], a[1]), a23 = f2(a[2], a[3]);
+                        q01 = f2_add(q01, f2_mul(a01, a01));
+                        q23 = f2_add(q23, f2_mul(a23, a23));
+                    } else if (!TAIL || i < NI - 1) {
+                        push2(m01, q01, f2(a[0], a[1]), r);
+                        push2(m23, q23, f2(a[2], a[3]), r);
+                    } else {
+                        // last step with masked lanes: keep the old state there
+                        f2_t nm01 = m01, nq01 = q01, nm23 = m23, nq23 = q23;
+                        push2(nm01, nq01, f2(a[0], a[1]), r);
+                        push2(nm23, nq23, f2(a[2], a[3]), r);
+                        float o[4], w[4], oq[4], wq[4];
+                        f2_split(m01, o[0], o[1]);
+                        f2_split(m23, o[2], o[3]);
+                        f2_split(nm01, w[0], w[1]);
+                        f2_split(nm23, w[2], w[3]);
+                        f2_split(q01, oq[0], oq[1]);
+                        f2_split(q23, oq[2], oq[3]);
+                        f2_split(nq01, wq[0], wq[1]);
+                        f2_split(nq23, wq[2], wq[3]);
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            o[s] = vlast[s] ? w[s] : o[s];
+                            oq[s] = vlast[s] ? wq[s] : oq[s];
+                        }
+                        m01 = f2(o[0], o[1]);
+                        m23 = f2(o[2], o[3]);
+                        q01 = f2(oq[0], oq[1]);
+                        q23 = f2(oq[2], oq[3]);
+                    }
+                });
             });
-        });
 
-        // this row has arrived: ask L2 for the warp's next row now, so that
-        // its DRAM reads overlap this row's fold, output pass and stores
-        if (u == 0 && row + kRowsThreads / 32 < r1) prefetch_l2(p.x + bn * p.sxB + nn * p.sxN, (uint64_t)D * 2);
+            // this row has arrived: ask L2 for the warp's next row now, so that
+            // its DRAM reads overlap this row's fold, output pass and stores
+            if (u == 0 && row + kRowsThreads / 32 < r1) prefetch_l2(p.x + bn * p.sxB + nn * p.sxN, (uint64_t)D * 2);
 
-        float mean, m2;
-        if constexpr (RMS) {
-            mean = 0.0f;
-            m2 = fold128_sum_s8(q01, q23);
-        } else {
-            fold128_s8(m01, q01, m23, q23, plan, mean, m2);
-        }
-        const float rstd = finish_rstd(m2, Df, p.eps);
+            float mean, m2;
+            if constexpr (RMS) {
+                mean = 0.0f;
+                m2 = fold128_sum_s8(q01, q23);
+            } else {
+                fold128_s8(m01, q01, m23, q23, plan, mean, m2);
+            }
+            const float rstd = finish_rstd(m2, Df, p.eps);
 
-        // pass 2: normalise, modulate, store
-        const uint16_t *scr = p.scale + b * p.s_scale_b + n * p.s_scale_n + c0;
-        const uint16_t *shr = p.shift + b * p.s_shift_b + n * p.s_shift_n + c0;
-        const uint32_t *ob = opsh + b * D + c0;  // OPSH: (op, shift) of the column pairs from c0 on
-        uint16_t *orow = p.out + row * (int64_t)D + c0;
-        uint8_t *orow8 = reinterpret_cast<uint8_t *>(p.out) + row * (int64_t)D + c0;  // E4M3
-        const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
-        // (e4m3: two copies of the pass, the quantiser chosen once per row;
-        // a choice per chunk inside the unrolled loop is much slower)
-        auto pass2 = [&](auto fastq) {
+            // pass 2: normalise, modulate, store
+            const uint16_t *scr = p.scale + b * p.s_scale_b + n * p.s_scale_n + c0;
+            const uint16_t *shr = p.shift + b * p.s_shift_b + n * p.s_shift_n + c0;
+            const uint32_t *ob = opsh + b * D + c0;  // OPSH: (op, shift) of the column pairs from c0 on
+            uint16_t *orow = p.out + row * (int64_t)D + c0;
+            uint8_t *orow8 = reinterpret_cast<uint8_t *>(p.out) + row * (int64_t)D + c0;  // E4M3
+            const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
 #pragma unroll
@@ -342,7 +363,10 @@ ln_rows_kernel(const RowsParams p) {
                             o[k] = add16x2<T>(mul16x2<T>(pack_rn<T>(y0, y1), op[k]), sh[k]);
                         }
                         if constexpr (E4M3) {
-                            if constexpr (decltype(fastq)::value) {
+                            constexpr int QF = decltype(qform)::value;
+                            if constexpr (QF == 2) {
+                                st4(orow8 + off, quant4_e4m3_plain<T>(o, qc));
+                            } else if constexpr (QF == 1) {
                                 st4(orow8 + off, quant4_e4m3_fast<T>(o, qc));
                             } else {
                                 st4(orow8 + off, quant4_e4m3_window<T>(o, qc));
@@ -353,15 +377,21 @@ ln_rows_kernel(const RowsParams p) {
                     }
                 }
             }
-        };
-        if (E4M3 && qc.fast) {
-            pass2(std::true_type{});
-        } else {
-            pass2(std::false_type{});
+            if (row + kRowsThreads / 32 < r1) load_row(row_x(bn, nn));
+            rb = bn;
+            rn = nn;
         }
-        if (row + kRowsThreads / 32 < r1) load_row(row_x(bn, nn));
-        rb = bn;
-        rn = nn;
+    };
+    if constexpr (E4M3) {
+        if (qc.plain) {
+            row_loop(std::integral_constant<int, 2>{});
+        } else if (qc.fast) {
+            row_loop(std::integral_constant<int, 1>{});
+        } else {
+            row_loop(std::integral_constant<int, 0>{});
+        }
+    } else {
+        row_loop(std::integral_constant<int, 0>{});
     }
 }
 

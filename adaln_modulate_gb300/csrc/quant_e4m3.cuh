@@ -46,11 +46,27 @@ __device__ __forceinline__ float div_by_recip(float a, float b, float r) {
 // |y / qs| < 2^-40: the code is a signed zero either way, and the sign comes
 // out right (q is RN(y r) or carries its sign).  Infinities become the
 // clamped bound (saturating), NaN stays NaN.
+//
+// Cheaper still (quant4_e4m3_plain): the code of the product RN(y p) alone,
+// for a multiplier p near 1 / qs whose codes equal those of RN(y / qs) for
+// every storage value.  For y = M 2^E (M the significand; a subnormal
+// normalises to one of the same M) the two are the scaled values
+// RN(M p) 2^E and RN(M / qs) 2^E, so it is enough to compare the two codes
+// for every significand M (128 for bf16, 1024 for fp16) and every E that
+// puts the quotient in [2^-12, 2^11): below that both codes are signed
+// zeros, above both are +-448.  Zeros, infinities and NaN need nothing
+// (RN(y p) is a signed zero, +-inf, NaN).  The check (quant_plain_share) is
+// run once per CTA, split over its threads, for p = r, then r -+ 1 ulp and
+// r -+ 2 ulp (quant_pick_plain); r itself fails when some quotient lies
+// within an ulp of an e4m3 rounding boundary, and every p fails for exact
+// ties (y = m s with m a midpoint) that the product rounds the other way.
 struct QuantE4M3 {
     float qs, qr, nqs;  // the scale, RN(1 / scale), -scale
     uint32_t lo2, hi2;  // the pattern window, in both 16-bit halves
     uint32_t nhi2;      // the upper bound's pattern with the sign bit set, in both halves
     bool fast;          // the scale is ordinary and positive: quant4_e4m3_fast applies
+    bool plain;         // quant4_e4m3_plain applies, with the multiplier rp (quant_pick_plain)
+    float rp;
 };
 
 template <DT T> __device__ __forceinline__ uint32_t pattern_ceil(float t);
@@ -91,7 +107,113 @@ __device__ __forceinline__ QuantE4M3 quant_setup(float qs) {
     c.fast = qs >= 0x1p-60f && qs <= 0x1p+60f && pattern_value<T>(hp) >= 1024.0f * qs;
     const uint32_t nh = (c.fast ? hp : 0u) | 0x8000u;
     c.nhi2 = nh | (nh << 16);
+    c.plain = false;
+    c.rp = c.qr;
     return c;
+}
+
+// q 2^j for a normal q whose product stays normal (exact)
+__device__ __forceinline__ float scale_pow2(float q, int j) {
+    return __uint_as_float(__float_as_uint(q) + ((uint32_t)j << 23));
+}
+
+// The multiplier candidate t of the plain-product search: r, r - 1 ulp,
+// r + 1 ulp, r - 2 ulp, r + 2 ulp (r > 0)
+constexpr int kPlainTries = 5;
+__device__ __forceinline__ float plain_candidate(float r, int t) {
+    const int k = ((t + 1) >> 1) * ((t & 1) ? -1 : 1);
+    return __uint_as_float(__float_as_uint(r) + (uint32_t)k);
+}
+
+// One thread's share of the plain-product check for the multiplier p:
+// significands M = 1 + i 2^-F (F = 7 for bf16, 10 for fp16), i = first,
+// first + stride, ...  True when, for each of them, RN(M p) 2^j and
+// RN(M / qs) 2^j have the same code for every j that puts RN(M / qs) 2^j in
+// [2^-12, 2^11).  The code of a value depends on its binade only through the
+// number of significand bits e4m3 keeps there: the binades [2^-11, 2^-10)
+// .. [2^-7, 2^-6) each keep their own number (zero threshold, subnormals),
+// the normal ones [2^-6, 2^8) all keep three and [2^8, 2^9) three with the
+// saturation at 448, so one binade stands for all the normal ones.  Near a
+// binade boundary both values round to the boundary's code.  With
+// 2^-60 <= qs <= 2^60 every value involved is a normal binary32.
+template <DT T>
+__device__ __forceinline__ bool quant_plain_share(const QuantE4M3 &c, float p, int first, int stride) {
+    constexpr int F = T == DT::BF16 ? 7 : 10;
+    constexpr int kBinades[7] = {-11, -10, -9, -8, -7, 0, 8};
+    if (!c.fast) return false;
+    bool ok = true;
+    for (int i = first; i < (1 << F); i += stride) {
+        const float M = 1.0f + (float)i * (1.0f / (float)(1 << F));
+        const float qe = __fdiv_rn(M, c.qs), q0 = __fmul_rn(M, p);
+        const int e = (int)((__float_as_uint(qe) >> 23) & 0xffu) - 127;
+#pragma unroll
+        for (int k = 0; k < 7; ++k) {
+            const int j = kBinades[k] - e;
+            const uint32_t two = __nv_cvt_float2_to_fp8x2(make_float2(scale_pow2(qe, j), scale_pow2(q0, j)),
+                                                          __NV_SATFINITE, __NV_E4M3);
+            ok &= ((two ^ (two >> 8)) & 0xffu) == 0u;
+        }
+    }
+    return ok;
+}
+
+// The last scale the search ran for on this device, per storage type, with
+// its outcome: the scale's bits in the high half, the multiplier's bits in
+// the low half (0: the product does not apply).  Written and read as one
+// 64-bit word, so a reader sees one search's outcome whole; a write by a
+// CTA of the current grid is seen by later grids (kernel boundaries order
+// it) and maybe by CTAs of this one, which is harmless either way: the
+// outcome for a scale is the same whoever computes it.  (Internal linkage:
+// each translation unit that includes this keeps its own.)
+static __device__ unsigned long long g_plain_memo[2];
+template <DT T> __device__ __forceinline__ unsigned long long plain_memo_load() {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(&g_plain_memo[T == DT::BF16 ? 0 : 1]) : "memory");
+    return v;
+}
+template <DT T> __device__ __forceinline__ void plain_memo_store(unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(&g_plain_memo[T == DT::BF16 ? 0 : 1]), "l"(v) : "memory");
+}
+__device__ __forceinline__ bool plain_memo_hit(unsigned long long m, const QuantE4M3 &c) {
+    return c.fast && (uint32_t)(m >> 32) == __float_as_uint(c.qs);
+}
+
+// The CTA's search for a plain-product multiplier: candidates r, r -+ 1 ulp,
+// r -+ 2 ulp in turn, each checked by all threads and closed by a barrier
+// (every thread of the CTA calls it, for an ordinary positive scale).
+// Returns the multiplier's bits, 0 if every candidate fails.  Out of line:
+// it runs only when the memo misses, and kept apart it leaves the kernel's
+// main path as it is.
+template <DT T>
+__device__ __noinline__ uint32_t quant_plain_search(float qs, float qr, int first, int stride) {
+    QuantE4M3 c{};
+    c.qs = qs;
+    c.qr = qr;
+    c.fast = true;
+    for (int t = 0; t < kPlainTries; ++t) {
+        const float p = plain_candidate(qr, t);
+        if (__syncthreads_and(quant_plain_share<T>(c, p, first, stride))) return __float_as_uint(p);
+    }
+    return 0u;
+}
+
+// The CTA's decision between the plain product and the other forms (every
+// thread of the CTA calls it, after a barrier that published memo_s: thread
+// 0's plain_memo_load()).  A memo hit takes the recorded outcome; a miss
+// searches and thread 0 records the outcome.  Sets c.plain and c.rp.
+template <DT T>
+__device__ __forceinline__ void quant_pick_plain(QuantE4M3 &c, const unsigned long long *memo_s, int first,
+                                                 int stride) {
+    const unsigned long long m = *memo_s;
+    uint32_t rp = 0u;
+    if (plain_memo_hit(m, c)) {
+        rp = (uint32_t)m;
+    } else if (c.fast) {
+        rp = quant_plain_search<T>(c.qs, c.qr, first, stride);
+        if (first == 0) plain_memo_store<T>(((unsigned long long)__float_as_uint(c.qs) << 32) | rp);
+    }
+    c.plain = rp != 0u;
+    c.rp = c.plain ? __uint_as_float(rp) : c.qr;
 }
 
 // (by value: the values stay in registers; the call is rare)
@@ -129,6 +251,21 @@ template <> __device__ __forceinline__ uint32_t neg_clamp16x2<DT::FP16>(uint32_t
     uint32_t r;
     asm("min.NaN.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(nb));
     return r;
+}
+
+// the e4m3 codes of 4 storage values (2 packed pairs), in memory order, when
+// the product alone gives them (c.plain)
+template <DT T>
+__device__ __forceinline__ uint32_t quant4_e4m3_plain(const uint32_t *o, const QuantE4M3 &c) {
+    const f2_t r2 = f2(c.rp, c.rp);
+    const f2_t p01 = f2_mul(f2(lo_f32<T>(o[0]), hi_f32<T>(o[0])), r2);
+    const f2_t p23 = f2_mul(f2(lo_f32<T>(o[1]), hi_f32<T>(o[1])), r2);
+    float q0, q1, q2, q3;
+    f2_split(p01, q0, q1);
+    f2_split(p23, q2, q3);
+    const uint32_t q01 = __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t q23 = __nv_cvt_float2_to_fp8x2(make_float2(q2, q3), __NV_SATFINITE, __NV_E4M3);
+    return (q01 & 0xffffu) | (q23 << 16);
 }
 
 // the e4m3 codes of 4 storage values (2 packed pairs), in memory order, for
@@ -177,7 +314,7 @@ __device__ __forceinline__ uint32_t quant4_e4m3_window(const uint32_t *o, const 
 
 template <DT T>
 __device__ __forceinline__ uint32_t quant4_e4m3(const uint32_t *o, const QuantE4M3 &c) {
-    return c.fast ? quant4_e4m3_fast<T>(o, c) : quant4_e4m3_window<T>(o, c);
+    return c.plain ? quant4_e4m3_plain<T>(o, c) : c.fast ? quant4_e4m3_fast<T>(o, c) : quant4_e4m3_window<T>(o, c);
 }
 
 }  // namespace adaln

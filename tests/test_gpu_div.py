@@ -29,7 +29,7 @@ def helper(tmp_path_factory):
     lib = ctypes.CDLL(so)
     lib.div_sweep.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong]
     lib.quant4_sweep.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int,
-                                 ctypes.c_int, ctypes.c_void_p]
+                                 ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     return lib
 
 
@@ -71,29 +71,45 @@ def _extreme_scales():
     return [2.0 ** -70, 2.0 ** 70, -0.03, -3.0, 100.0, 3.0e4]
 
 
-@pytest.mark.parametrize("window", [0, 1], ids=["as_picked", "window_form"])
+@pytest.mark.parametrize("form,memo", [(0, 0), (0, 1), (1, 0), (2, 0)],
+                         ids=["as_picked", "as_picked_with_memo", "window_form", "corrected_form"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-def test_quantiser_codes_equal_the_oracle(helper, dtype, window):
+def test_quantiser_codes_equal_the_oracle(helper, dtype, form, memo):
     """The rows kernel's 4-wide quantisers against the oracle's IEEE division
     and e4m3 encoder, for every 16-bit pattern (NaN codes compared as NaN):
-    the form the kernel picks for each scale (the branch-free one: clamped
-    magnitudes and the correction on -y; or the window form: the product with
-    RN(1/s) and the exact quotient near e4m3 boundaries), and the window form
-    forced for every scale."""
+    the form the kernel picks for each scale (the plain product RN(y r) when
+    the per-CTA check over all significands passes; else, for an ordinary
+    positive scale, clamped magnitudes and Markstein's correction on -y; else
+    the window form: the product and the exact quotient near e4m3
+    boundaries), and the window and corrected forms forced.  With the memo
+    each scale runs twice: the first call searches (the previous scale is
+    another), the second takes the memo's outcome."""
     pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     yg = torch.from_numpy(pats.view(np.int16).copy()).cuda()
     codes = torch.empty(65536, dtype=torch.uint8, device="cuda")
-    fast = torch.zeros(1, dtype=torch.int32, device="cuda")
-    picked = set()
-    for s in _scales() + _tie_scales() + _extreme_scales():
-        assert helper.quant4_sweep(yg.data_ptr(), s, codes.data_ptr(), 65536 // 4, int(dtype == "fp16"), window,
-                                   fast.data_ptr()) == 0
+    picked = torch.zeros(1, dtype=torch.int32, device="cuda")
+    plain_for = {}
+    scales = _scales() + _tie_scales() + _extreme_scales()
+    for s in [v for v in scales for _ in range(1 + memo)]:
+        assert helper.quant4_sweep(yg.data_ptr(), s, codes.data_ptr(), 65536 // 4, int(dtype == "fp16"), form, memo,
+                                   picked.data_ptr()) == 0
         expect_fast = 2.0 ** -60 <= s <= 2.0 ** 60 and (dtype == "bf16" or s <= 65504.0 / 1024.0)
-        assert bool(fast.item()) == expect_fast, s
-        picked.add(expect_fast and not window)
+        pk = int(picked.item())
+        assert bool(pk & 1) == expect_fast, s
+        assert not (pk & 2) or expect_fast, s
+        assert plain_for.get(s, bool(pk & 2)) == bool(pk & 2), s   # the memo's outcome is the search's
+        plain_for[s] = bool(pk & 2)
+        if form == 2 and not expect_fast:
+            continue  # the corrected form is defined for ordinary positive scales only
         got = codes.cpu().numpy()
         ref = oracle.quant_e4m3(pats, s, dtype)
         nan_r = (ref & 0x7F) == 0x7F
         assert np.array_equal((got & 0x7F) == 0x7F, nan_r), s
         assert np.array_equal(got[~nan_r], ref[~nan_r]), (s, int((got[~nan_r] != ref[~nan_r]).sum()))
-    assert picked == ({True, False} if not window else {False})
+    # exact ties that the product rounds the other way (y = m s, s = 7, 13)
+    # defeat every multiplier tried; 0.03 takes r - 1 ulp; nearly every other
+    # ordinary scale takes the product
+    assert not plain_for[7.0] and not plain_for[13.0]
+    assert plain_for[float(np.float32(0.03))]
+    fast_scales = [s for s in _scales() if 2.0 ** -60 <= s <= 2.0 ** 60 and (dtype == "bf16" or s <= 63.97)]
+    assert sum(plain_for[s] for s in fast_scales) >= 0.9 * len(fast_scales)

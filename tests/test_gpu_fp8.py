@@ -68,6 +68,16 @@ def test_scales_in_range_and_saturating(ad, qscale):
         assert ((ref & 0x7F) == 0x7E).any()   # saturated codes present
 
 
+@pytest.mark.parametrize("dtype,qscale", [("bf16", 0.03), ("bf16", 7.0), ("bf16", -0.05), ("fp16", 0.03),
+                                          ("fp16", 13.0), ("fp16", 100.0)])
+def test_each_quantiser_form(ad, dtype, qscale):
+    # the rows kernel's output pass in each of its forms: the plain product
+    # (0.03, with the multiplier RN(1/s) - 1 ulp), the clamped correction
+    # (7 and 13: exact ties defeat every multiplier), the window form (a
+    # negative scale; fp16 with a scale above 63.97)
+    case(ad, 2, 40, 3072, qscale, dtype, seed=int(abs(qscale) * 100) + 5, expect="rows")
+
+
 @pytest.mark.parametrize("D,expect", [(5120, "rows"), (6144, "rows"), (8192, "generic")])
 def test_large_d(ad, D, expect):
     case(ad, 2, 11, D, 0.02, seed=D + 1, expect=expect)
