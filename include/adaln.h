@@ -239,6 +239,16 @@ adaln_status adaln_can_qk_rmsnorm(const void *q_out, const void *q, int64_t rows
  * Numerics: y exactly as adaln_ln_modulate stores it, then one IEEE
  * binary32 division by *qscale, round to nearest even to e4m3, saturating
  * at +-448 (infinities included); NaN stays NaN.
+ * Cost: the rows kernel gets these codes from the product y * p alone when
+ * a check over every significand of the storage type shows that, for a
+ * multiplier p within 2 ulp of 1 / qscale, the product gives the division's
+ * code for every 16-bit value.  Each CTA runs that check (about a
+ * microsecond) only when the device's record of the last checked scale (one
+ * per storage type, kept in device memory by the library) holds a
+ * different scale, so calls that reuse a scale skip it; calls that
+ * alternate scales on one device run it every time.  Scales that no
+ * multiplier serves take an exact correction (a few operations more per
+ * element).  The bits are the same in every case.
  * ---------------------------------------------------------------------- */
 adaln_status adaln_ln_modulate_fp8(void *out, const void *qscale, const void *x,
                                   int64_t B, int64_t N, int64_t D,
