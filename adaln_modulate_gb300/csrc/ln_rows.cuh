@@ -237,9 +237,11 @@ ln_rows_kernel(const RowsParams p) {
 
             // pass 1: Welford (or the sum of squares) of lanes (s0, s1) and
             // (s2, s3), one f32x2 op each
-            f2_t m01 = f2(0.f, 0.f), q01 = m01, m23 = m01, q23 = m01;
-            const uint16_t *gr = nullptr;  // GATE: this row's gate row (or value)
-            uint32_t gs = 0;               // GATE_SCALAR: the value in both halves
+            // (each instantiation uses some of these: the rest are marked maybe_unused)
+            f2_t m01 = f2(0.f, 0.f), q01 = m01, q23 = m01;
+            [[maybe_unused]] f2_t m23 = m01;
+            [[maybe_unused]] const uint16_t *gr = nullptr;  // GATE: this row's gate row (or value)
+            [[maybe_unused]] uint32_t gs = 0;               // GATE_SCALAR: the value in both halves
             if constexpr (GATE) gr = p.gate + b * p.s_gate_b + n * p.s_gate_n;
             if constexpr (GM == GATE_SCALAR) {
                 const uint32_t g1 = ldg_u16(gr);
@@ -328,11 +330,12 @@ ln_rows_kernel(const RowsParams p) {
             const float rstd = finish_rstd(m2, Df, p.eps);
 
             // pass 2: normalise, modulate, store
-            const uint16_t *scr = p.scale + b * p.s_scale_b + n * p.s_scale_n + c0;
-            const uint16_t *shr = p.shift + b * p.s_shift_b + n * p.s_shift_n + c0;
-            const uint32_t *ob = opsh + b * D + c0;  // OPSH: (op, shift) of the column pairs from c0 on
-            uint16_t *orow = p.out + row * (int64_t)D + c0;
-            uint8_t *orow8 = reinterpret_cast<uint8_t *>(p.out) + row * (int64_t)D + c0;  // E4M3
+            [[maybe_unused]] const uint16_t *scr = p.scale + b * p.s_scale_b + n * p.s_scale_n + c0;
+            [[maybe_unused]] const uint16_t *shr = p.shift + b * p.s_shift_b + n * p.s_shift_n + c0;
+            // OPSH: (op, shift) of the column pairs from c0 on
+            [[maybe_unused]] const uint32_t *ob = opsh + b * D + c0;
+            [[maybe_unused]] uint16_t *orow = p.out + row * (int64_t)D + c0;
+            [[maybe_unused]] uint8_t *orow8 = reinterpret_cast<uint8_t *>(p.out) + row * (int64_t)D + c0;  // E4M3
             const f2_t mm = f2(mean, mean), rr = f2(rstd, rstd);
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
